@@ -1,0 +1,451 @@
+"""Benchmark of the routed MoE FFN hot path on GB300 (one JSON line on stdout, rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one full forward (route grouping when T > 1, gate/up + SwiGLU, down + combine) over one
+batch of the named workload with its inputs resident in HBM. Default workload: ``fp8_decode``
+(T=1, H=7168, I=2048, E=256, top-8, E4M3 with 128x128 block scales). Between timed steps a
+buffer of twice the L2 size is written (outside the timed events) and the route set rotates
+through 8 seeded draws, so every step streams its experts from HBM.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path does not
+shard: replicas only, no collective on the data path); the barrier and the max over ranks are
+only for timing. ``--impl reference`` times the FP64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_expert_ffn_histogram_gb300 import inputs  # noqa: E402
+
+METRIC = "MoE FFN tokens/s; effective weight GB/s as % of GB300 HBM peak"
+UNIT = "tokens/s"
+N_ROUTE_SETS = 8
+
+
+# ---- distributed (replicas only) -------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Largest value over all ranks (the slowest replica sets the job time)."""
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---- measured peaks ------------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---- clocks during the timed region ----------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.lines = []
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            if uuid and not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+        except Exception:
+            uuid = None
+        self.sel = ["--id=" + uuid] if uuid else []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---- algorithmic bytes -----------------------------------------------------------------------------
+
+def matrix_bytes(fmt, n, k):
+    if fmt == "fp8":
+        return n * k + (n // 128) * (k // 128) * 4
+    return n * k // 2 + n * (k // 16)
+
+
+def alg_bytes(wl):
+    """Per call: distinct selected experts' codes + scales of the three projections, plus x,
+    out, ids and weights (and the small f16 activation round trip through the workspace)."""
+    ids = wl.ids.cpu().numpy().reshape(-1)
+    distinct = len({int(e) for e in ids if 0 <= e < wl.E})
+    P = wl.T * wl.topk
+    w_gu = distinct * 2 * matrix_bytes(wl.fmt, wl.I, wl.H)
+    w_d = distinct * matrix_bytes(wl.fmt, wl.H, wl.I)
+    act = P * wl.I * 2 + P * (wl.I // 64) * 4
+    x = wl.T * wl.H * 2
+    out = wl.T * wl.H * 2
+    idw = P * 8
+    return dict(distinct=distinct, gate_up=w_gu + x + act, down=w_d + act + out + idw,
+                total=w_gu + w_d + x + out + idw, weights=w_gu + w_d)
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_expert_ffn_histogram_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config, kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on these sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(config, {}).get(kernel)
+    if not ent or ent.get("source_sha") != kernel_source_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---- the CPU oracle (baseline / reference arm) ------------------------------------------------------
+
+def oracle_sample(name, route_set, device, n_tokens=None):
+    """One bounded oracle sample of the workload: the sampled tokens' selected experts are
+    generated (same seeded bytes as the full bank) and copied to the host, outside the timing."""
+    c = inputs.CONFIGS[name]
+    tmp = inputs.make_workload(name, device="cpu", bank=object(), route_set=route_set)
+    T = tmp.T if n_tokens is None else min(n_tokens, tmp.T)
+    ids = tmp.ids[:T].numpy()
+    used = sorted({int(e) for e in ids.reshape(-1) if 0 <= e < c["E"]})
+    remap = {e: i for i, e in enumerate(used)}
+    sub_ids = np.vectorize(lambda e: remap.get(int(e), -1))(ids).astype(np.int32)
+    bank = inputs.make_bank(name, device=device, experts=used).numpy()
+    x = tmp.x[:T].view(torch.int16).numpy().view(np.uint16)
+    wts = tmp.wts[:T].numpy()
+    return dict(x=x, ids=sub_ids, wts=wts, bank=bank, fmt=c["fmt"], T=T)
+
+
+def run_oracle(sample, limit=inputs.LIMIT):
+    import oracle
+    fn = oracle.moe_fp8 if sample["fmt"] == "fp8" else oracle.moe_nvfp4
+    t0 = time.perf_counter()
+    fn(sample["x"], sample["ids"], sample["wts"], sample["bank"], limit)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(name, device, budget_s=20.0):
+    """Oracle tokens/s on a bounded sample of the workload (about budget_s of CPU work)."""
+    import oracle
+    oracle.build()
+    c = inputs.CONFIGS[name]
+    n_tok = 1 if c["T"] <= 8 else 2
+    secs, toks, samples = 0.0, 0, 0
+    rs = 0
+    while samples < 8 and (secs < budget_s or samples == 0):
+        s = oracle_sample(name, rs, device, n_tokens=min(c["T"], n_tok))
+        secs += run_oracle(s)
+        toks += s["T"]
+        samples += 1
+        rs += 1
+        if secs > budget_s * 0.5 and samples >= 1 and secs / samples * (samples + 1) > budget_s:
+            break
+    return {"value": toks / secs, "unit": UNIT, "cores": oracle.hardware_threads(),
+            "kind": "oracle",
+            "sample": f"{toks} token(s) of {name} over {samples} seeded route set(s), "
+                      f"FP64 C++ oracle, {secs:.1f} s"}
+
+
+# ---- our arm ---------------------------------------------------------------------------------------
+
+def make_route_sets(name, device, bank, E=None):
+    return [inputs.make_workload(name, device=device, bank=bank, route_set=i, E=E)
+            for i in range(N_ROUTE_SETS)]
+
+
+def bench_ours(args):
+    from moe_expert_ffn_histogram_gb300 import _build, capi
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    _build.build()
+    capi.load()
+
+    name = args.config
+    c = inputs.CONFIGS[name]
+    E = c["E"] if args.bank_experts is None else args.bank_experts
+    bank = inputs.make_bank(name, dev, experts=None if E == c["E"] else range(E))
+    sets = make_route_sets(name, dev, bank, E)
+    wl0 = sets[0]
+    fmt_code = capi.FMT_FP8 if c["fmt"] == "fp8" else capi.FMT_NVFP4
+    ws = capi.alloc_workspace(wl0.T, wl0.H, wl0.I, wl0.E, wl0.topk, fmt_code, dev)
+    out = torch.empty(wl0.T, wl0.H, dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd(wl, o=out):
+        capi.forward(wl.x, wl.ids, wl.wts, wl.bank, wl.limit, out=o, workspace=ws)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        fwd(sets[i % N_ROUTE_SETS])
+    torch.cuda.synchronize()
+
+    # ---- timed region: whole forward per step, device events on the launching stream
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd(sets[i % N_ROUTE_SETS])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # ---- per-kernel durations (same kernels, called stage by stage) for the roofline
+    T = wl0.T
+    stage_ms = {"plan": [], "gate_up": [], "down_combine": []}
+    if T <= 8:
+        for i in range(args.steps):
+            wl = sets[i % N_ROUTE_SETS]
+            flush.zero_()
+            e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+            e0.record(stream)
+            capi.plan(wl.ids, wl.H, wl.I, wl.E, fmt_code, ws)
+            e1.record(stream)
+            capi.gate_up(wl.x, wl.ids, wl.bank, wl.limit, ws)
+            e2.record(stream)
+            capi.down_combine(wl.ids, wl.wts, wl.bank, out, ws)
+            e3.record(stream)
+            torch.cuda.synchronize()
+            stage_ms["plan"].append(e0.elapsed_time(e1))
+            stage_ms["gate_up"].append(e1.elapsed_time(e2))
+            stage_ms["down_combine"].append(e2.elapsed_time(e3))
+    clk = clocks.stop()
+
+    # ---- end to end through the public API: pinned host inputs in, result out, every step
+    hx = [s.x.cpu().pin_memory() for s in sets]
+    hids = [s.ids.cpu().pin_memory() for s in sets]
+    hw = [s.wts.cpu().pin_memory() for s in sets]
+    hout = torch.empty(T, wl0.H, dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(wl0.x)
+    dids = torch.empty_like(wl0.ids)
+    dw = torch.empty_like(wl0.wts)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        j = i % N_ROUTE_SETS
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dx.copy_(hx[j], non_blocking=True)
+        dids.copy_(hids[j], non_blocking=True)
+        dw.copy_(hw[j], non_blocking=True)
+        capi.forward(dx, dids, dw, bank, inputs.LIMIT, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    h2d = wl0.x.numel() * 2 + wl0.ids.numel() * 4 + wl0.wts.numel() * 4
+    d2h = T * wl0.H * 2
+
+    # ---- aggregate (replicas: units add up, the slowest rank sets the time)
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    units = sum_over_ranks(float(T * args.steps), world, dev)
+    value = units / total_s
+    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world, dev)
+    e2e_value = sum_over_ranks(float(T * args.steps), world, dev) / e2e_s
+
+    peak, peak_kind = load_peaks()
+    by = [alg_bytes(s) for s in sets]
+    mean_total = statistics.mean(b["total"] for b in by)
+    ms = statistics.mean(step_ms)
+    call_gbs = mean_total / (ms * 1e-3) / 1e9
+    roof = None
+    if stage_ms["gate_up"]:
+        gu_ms = statistics.mean(stage_ms["gate_up"])
+        gu_bytes = statistics.mean(b["gate_up"] for b in by)
+        ach = gu_bytes / (gu_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "gate_up_kernel", "achieved": round(ach, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "traffic": profiled_traffic(name, "gate_up"),
+                "alg_bytes_per_launch": int(gu_bytes), "avg_launch_us": round(gu_ms * 1e3, 2)}
+    launches_per_step = (0 if T == 1 else 1) + 2 if T <= 8 else 3 * ((T + 7) // 8)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3/bf16->f32" if c["fmt"] == "fp8" else "e2m1/bf16->f32",
+        "data": "synthetic (seeded N(0,0.02) weights quantised, N(0,1) bf16 activations)",
+        "config": {"workload": name, "T": T, "H": c["H"], "I": c["I"], "E": E, "topk": 8,
+                   "format": "fp8_e4m3_block128" if c["fmt"] == "fp8" else "nvfp4",
+                   "routes": c["routes"], "route_sets": N_ROUTE_SETS,
+                   "l2": "flushed between steps (write of 2x L2 outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "effective_weight_gbs": round(call_gbs, 1),
+        "hbm_frac_of_peak": round(call_gbs / peak, 4),
+        "p50_ms": round(float(np.percentile(step_ms, 50)), 5),
+        "p99_ms": round(float(np.percentile(step_ms, 99)), 5),
+        "stage_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in stage_ms.items() if v},
+        "roofline": roof,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 5)},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(name, dev, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    name = args.config
+    c = inputs.CONFIGS[name]
+    gen_dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    n_tok = 1 if c["T"] <= 8 else 2
+    samples = [oracle_sample(name, i % N_ROUTE_SETS, gen_dev, n_tokens=n_tok)
+               for i in range(min(N_ROUTE_SETS, args.warmup + args.steps))]
+    for i in range(args.warmup):
+        run_oracle(samples[i % len(samples)])
+    secs, toks = [], 0
+    for i in range(args.steps):
+        s = samples[i % len(samples)]
+        secs.append(run_oracle(s))
+        toks += s["T"]
+    value = toks / sum(secs)
+    sample_desc = f"{n_tok} token(s) of {name} per step (bounded sample), FP64 C++ oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.mean(secs) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "T": c["T"], "H": c["H"], "I": c["I"], "E": c["E"],
+                   "topk": 8, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.hardware_threads(),
+                         "kind": "oracle", "sample": sample_desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="fp8_decode", choices=sorted(inputs.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--bank-experts", type=int, default=None,
+                    help="use only the first N experts of the bank (small profiling captures)")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps, always
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

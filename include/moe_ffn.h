@@ -1,0 +1,190 @@
+/*
+ * moe_ffn.h - C ABI of the GB300 (sm_103a) routed mixture-of-experts FFN library
+ * (libmoe_ffn_gb300.so).
+ *
+ * The operation (one MoE FFN site, top-k routing):
+ *
+ *   for each token t and slot k with expert e = topk_ids[t][k]:
+ *       g = Wg[e] . x[t]        u = Wu[e] . x[t]                      (gate, up: [I] each)
+ *       a = silu(min(g, limit)) * clamp(u, -limit, limit)             (clamped SwiGLU)
+ *       y = Wd[e] . a                                                  (down: [H])
+ *   out[t] = sum_{k = 0 .. topk-1, in slot order} topk_weights[t][k] * y(t, k)   -> bf16
+ *
+ * Sources: the per-expert chain is "memra-engine 0.108.0 src/bin/ep_step_fp8_gate.rs",
+ * `reference_expert`; the asymmetric clamp is "spark_model layers/glm5next_mlp/forward.rs",
+ * `swiglu_rows`; the slot-order combine is ep_step_fp8_gate.rs, `combine_down_rows_host`.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, except where a comment
+ *     says otherwise. The library allocates nothing, owns nothing, and keeps no state between
+ *     calls. Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream) and the function returns after enqueueing; nothing is synchronised.
+ *   - Argument checks are synchronous: on any MOE_ERR_* return nothing has been enqueued, except
+ *     MOE_ERR_CUDA, which reports a launch failure (work before the failing launch may be queued).
+ *   - Route ids: -1 marks an unfilled slot and contributes exactly 0. Any other id outside
+ *     [0, E) also contributes 0 and ORs bit 0 (MOE_ERRBIT_BAD_ID) into *err when err != NULL.
+ *     err is never cleared by the library. Duplicate ids within one token are legal and summed.
+ *   - Outputs are a deterministic function of the inputs: no floating-point atomics, fixed
+ *     reduction order. `out` must not alias x, the weights or the workspace.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Shapes: 1 <= topk <= 8; H and I are multiples of 128; E >= 1.
+ */
+#ifndef MOE_FFN_GB300_H
+#define MOE_FFN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_NULL = -1,        /* a required pointer is NULL                                   */
+    MOE_ERR_SHAPE = -2,       /* T < 1, topk outside 1..8, H or I not a positive multiple of 128,
+                                 E < 1, or a size too large for the tier                       */
+    MOE_ERR_WORKSPACE = -3,   /* workspace NULL or smaller than moe_workspace_bytes()         */
+    MOE_ERR_VALUE = -4,       /* limit is NaN or <= 0 (use +INFINITY for "no clamp"), or a
+                                 scale_2 that is not finite                                    */
+    MOE_ERR_CUDA = -5,        /* a kernel launch or attribute call failed                      */
+    MOE_ERR_UNSUPPORTED = -6, /* shape outside what this build's kernels cover                 */
+    MOE_ERR_ALIGN = -7        /* x, out or a weight/scale array is not 16-byte aligned          */
+} moe_status;
+
+typedef enum {
+    MOE_FMT_FP8_E4M3_B128 = 1, /* E4M3 codes + one fp32 scale per 128x128 block              */
+    MOE_FMT_NVFP4 = 2          /* packed E2M1 + E4M3 scale per 16 elements + fp32 scale_2     */
+} moe_format;
+
+#define MOE_ERRBIT_BAD_ID 1
+
+/*
+ * moe_workspace_bytes - device scratch needed by moe_fp8_forward / moe_nvfp4_forward for a call
+ * with these sizes (and any smaller T). A pure function of its arguments; 0 on invalid sizes.
+ * The workspace is fully rewritten by every call before it is read, so it needs no clearing.
+ * Sizing idea: "spark_model layers/glm5next_mlp/forward.rs", `mlp_ws_bytes` (scratch sized once
+ * for the widest call a site can make).
+ */
+MOE_API size_t moe_workspace_bytes(int T, int H, int I, int E, int topk, int fmt);
+
+/*
+ * moe_route_permute - route histogram and stable counting-sort of (token, slot) pairs by expert.
+ *
+ *   topk_ids        [T][topk] int32, row-major.
+ *   counts          [E]       out: number of pairs routed to each expert.
+ *   offsets         [E+1]     out: exclusive prefix sum of counts; offsets[E] = routed pairs.
+ *   sorted_pair     [T*topk]  out: sorted_pair[offsets[e] + r] = the r-th pair p = t*topk + k
+ *                             (ascending p) with topk_ids[p] == e; entries from offsets[E] on
+ *                             are -1.
+ *   pair_to_sorted  [T*topk]  out: inverse of sorted_pair; -1 for pairs that are not routed.
+ *   err             nullable; bit 0 set on an id outside [-1, E).
+ *
+ * Equal keys keep ascending pair order, so every output is unique and bit-exact.
+ * Source: "spark_model layers/glm5next_mlp/forward.rs", `Glm5NextMlpWorkspace` (sorted token ids,
+ * expert_offsets[E+1], token_to_perm) and the `moe_sort_by_expert` step of `forward_moe`.
+ * Limits: E <= 4096 (MOE_ERR_UNSUPPORTED beyond). One launch, no host synchronisation.
+ */
+MOE_API int moe_route_permute(const int32_t* topk_ids, int T, int topk, int E, int32_t* counts,
+                      int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,
+                      int32_t* err, void* stream);
+
+/*
+ * moe_fp8_forward - routed MoE FFN with E4M3 weights and one fp32 scale per 128x128 block.
+ *
+ *   x             [T][H]      bf16 activations.
+ *   topk_ids      [T][topk]   int32 expert ids.
+ *   topk_weights  [T][topk]   fp32 router weights.
+ *   w_gate, w_up  [E][I][H]   uint8 E4M3 codes (K = H contiguous);
+ *   s_gate, s_up  [E][I/128][H/128] fp32 block scales.
+ *   w_down        [E][H][I]   uint8 E4M3 codes;  s_down [E][H/128][I/128] fp32.
+ *                 Dequantised weight W[e][n][k] = e4m3(code) * s[e][n/128][k/128]
+ *                 ("memra-engine 0.108.0 src/bin/ep_step_fp8_gate.rs", `expert_matrix`).
+ *   limit         SwiGLU clamp (> 0; +INFINITY = no clamp).
+ *   out           [T][H]      bf16, fully written (zero for a token with no routed slot).
+ *   workspace     >= moe_workspace_bytes(T, H, I, E, topk, MOE_FMT_FP8_E4M3_B128) bytes,
+ *                 256-byte aligned.
+ *
+ * Arithmetic: weights decode exactly to f16, activations are carried as f16 with a power-of-two
+ * scale per token (and per 64-wide block of the activation a), products accumulate in fp32, the
+ * combine runs in slot order in fp32, and the result is rounded once to bf16.
+ */
+MOE_API int moe_fp8_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
+                    const int32_t* topk_ids, const float* topk_weights,
+                    const uint8_t* w_gate, const float* s_gate,
+                    const uint8_t* w_up, const float* s_up,
+                    const uint8_t* w_down, const float* s_down,
+                    float limit, uint16_t* out, void* workspace, size_t workspace_bytes,
+                    int32_t* err, void* stream);
+
+/*
+ * moe_nvfp4_forward - routed MoE FFN with NVFP4 (W4A16) weights.
+ *
+ *   w_gate, w_up  [E][I][H/2]   packed E2M1 codes: element 2j in the low nibble of byte j.
+ *   sf_gate, sf_up [E][I][H/16] E4M3 scale bytes, one per 16 consecutive K elements.
+ *   w_down        [E][H][I/2];  sf_down [E][H][I/16].
+ *   scale2_*      one fp32 per projection, passed BY VALUE.
+ *                 W[e][n][k] = e2m1(nibble) * e4m3(sf[e][n][k/16]) * scale_2
+ *                 ("memra-engine 0.131.0 src/dsv4_ep.rs", `chain`: wstride = inter*hidden/2,
+ *                 sstride = inter*hidden/16; "spark_model layers/glm5next_mlp/forward.rs",
+ *                 `w4a16_gemv`: scale_2 is a by-value scalar).
+ * Everything else as moe_fp8_forward.
+ */
+MOE_API int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
+                      const int32_t* topk_ids, const float* topk_weights,
+                      const uint8_t* w_gate, const uint8_t* sf_gate, float scale2_gate,
+                      const uint8_t* w_up, const uint8_t* sf_up, float scale2_up,
+                      const uint8_t* w_down, const uint8_t* sf_down, float scale2_down,
+                      float limit, uint16_t* out, void* workspace, size_t workspace_bytes,
+                      int32_t* err, void* stream);
+
+/*
+ * Stage entry points. moe_*_forward is exactly moe_plan (when T > 1), then moe_*_gate_up, then
+ * moe_*_down_combine, on one stream. They are exported so that a caller (or a profiler) can
+ * time or interleave the stages; each takes the same arguments as the forward call it belongs
+ * to and the same workspace, and must be called in that order for one forward.
+ *
+ * moe_plan            - groups the routed (token, slot) pairs by expert into the workspace
+ *                       (one launch; a no-op for T == 1, where slot k is group k).
+ * moe_*_gate_up       - dequant-fused gate and up projections for every group, clamped SwiGLU
+ *                       fused in; writes the activation a (f16, per-64 power-of-two scales) to
+ *                       the workspace.
+ * moe_*_down_combine  - dequant-fused down projection fused with the slot-order weighted
+ *                       combine; writes out.
+ */
+MOE_API int moe_plan(int T, int H, int I, int E, int topk, int fmt, const int32_t* topk_ids,
+             void* workspace, size_t workspace_bytes, int32_t* err, void* stream);
+
+MOE_API int moe_fp8_gate_up(const uint16_t* x, int T, int H, int I, int E, int topk,
+                    const int32_t* topk_ids, const uint8_t* w_gate, const float* s_gate,
+                    const uint8_t* w_up, const float* s_up, float limit, void* workspace,
+                    size_t workspace_bytes, int32_t* err, void* stream);
+
+MOE_API int moe_fp8_down_combine(int T, int H, int I, int E, int topk, const int32_t* topk_ids,
+                         const float* topk_weights, const uint8_t* w_down, const float* s_down,
+                         uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+MOE_API int moe_nvfp4_gate_up(const uint16_t* x, int T, int H, int I, int E, int topk,
+                      const int32_t* topk_ids, const uint8_t* w_gate, const uint8_t* sf_gate,
+                      float scale2_gate, const uint8_t* w_up, const uint8_t* sf_up,
+                      float scale2_up, float limit, void* workspace, size_t workspace_bytes,
+                      int32_t* err, void* stream);
+
+MOE_API int moe_nvfp4_down_combine(int T, int H, int I, int E, int topk, const int32_t* topk_ids,
+                           const float* topk_weights, const uint8_t* w_down,
+                           const uint8_t* sf_down, float scale2_down, uint16_t* out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Library build identification: the compiled CUDA architecture string (e.g. "sm_103a"). */
+MOE_API const char* moe_build_arch(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_FFN_GB300_H */

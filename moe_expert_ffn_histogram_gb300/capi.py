@@ -1,0 +1,251 @@
+"""Thin Python binding of libmoe_ffn_gb300 (include/moe_ffn.h), argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module checks tensor
+dtypes/devices/contiguity, passes raw pointers and the current CUDA stream, and turns a non-zero
+status into an exception. There is no fallback: if the library is missing it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_WORKSPACE",
+          -4: "MOE_ERR_VALUE", -5: "MOE_ERR_CUDA", -6: "MOE_ERR_UNSUPPORTED",
+          -7: "MOE_ERR_ALIGN"}
+FMT_FP8 = 1
+FMT_NVFP4 = 2
+ERRBIT_BAD_ID = 1
+
+EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_nvfp4_forward",
+            "moe_plan", "moe_fp8_gate_up", "moe_fp8_down_combine", "moe_nvfp4_gate_up",
+            "moe_nvfp4_down_combine", "moe_build_arch")
+
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code} ({STATUS.get(code, 'unknown')})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Load the in-tree shared library. Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build() "
+                           "(nvcc, sm_103a); there is no CPU fallback")
+    lib = ctypes.CDLL(p)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.moe_workspace_bytes.restype = sz
+    lib.moe_workspace_bytes.argtypes = [i32] * 6
+    lib.moe_route_permute.restype = i32
+    lib.moe_route_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.moe_fp8_forward.restype = i32
+    lib.moe_fp8_forward.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                    f32, vp, vp, sz, vp, vp]
+    lib.moe_nvfp4_forward.restype = i32
+    lib.moe_nvfp4_forward.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, vp,
+                                      f32, vp, vp, f32, f32, vp, vp, sz, vp, vp]
+    lib.moe_plan.restype = i32
+    lib.moe_plan.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
+    lib.moe_fp8_gate_up.restype = i32
+    lib.moe_fp8_gate_up.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp, sz,
+                                    vp, vp]
+    lib.moe_fp8_down_combine.restype = i32
+    lib.moe_fp8_down_combine.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_nvfp4_gate_up.restype = i32
+    lib.moe_nvfp4_gate_up.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, f32, vp, vp, f32,
+                                      f32, vp, sz, vp, vp]
+    lib.moe_nvfp4_down_combine.restype = i32
+    lib.moe_nvfp4_down_combine.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, vp,
+                                           sz, vp]
+    lib.moe_build_arch.restype = ctypes.c_char_p
+    lib.moe_build_arch.argtypes = []
+    if path is None:
+        _lib = lib
+    return lib
+
+
+# ---- marshalling helpers -------------------------------------------------------------------------
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(device, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+# ---- public API ----------------------------------------------------------------------------------
+
+def workspace_bytes(T: int, H: int, I: int, E: int, topk: int, fmt: int) -> int:
+    return int(load().moe_workspace_bytes(T, H, I, E, topk, fmt))
+
+
+def alloc_workspace(T, H, I, E, topk, fmt, device) -> torch.Tensor:
+    n = workspace_bytes(T, H, I, E, topk, fmt)
+    if n == 0:
+        raise ValueError("invalid sizes for moe_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)   # caching allocator: 256-B aligned
+
+
+def route_permute(ids: torch.Tensor, num_experts: int, err: Optional[torch.Tensor] = None,
+                  stream=None):
+    """Stable counting sort of (token, slot) pairs by expert (moe_route_permute)."""
+    dev = ids.device
+    _need(ids, "ids", torch.int32, dev)
+    T, topk = ids.shape
+    P = T * topk
+    counts = torch.empty(num_experts, dtype=torch.int32, device=dev)
+    offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    sorted_pair = torch.empty(P, dtype=torch.int32, device=dev)
+    pair_to_sorted = torch.empty(P, dtype=torch.int32, device=dev)
+    if err is not None:
+        _need(err, "err", torch.int32, dev)
+    rc = load().moe_route_permute(_ptr(ids), T, topk, num_experts, _ptr(counts), _ptr(offsets),
+                                  _ptr(sorted_pair), _ptr(pair_to_sorted), _ptr(err),
+                                  _stream(dev, stream))
+    _check("moe_route_permute", rc)
+    return dict(counts=counts, offsets=offsets, sorted_pair=sorted_pair,
+                pair_to_sorted=pair_to_sorted)
+
+
+def _common(x, ids, wts, out, workspace, err, fmt, E, I):
+    dev = x.device
+    _need(x, "x", torch.bfloat16, dev)
+    _need(ids, "topk_ids", torch.int32, dev)
+    _need(wts, "topk_weights", torch.float32, dev)
+    T, H = x.shape
+    topk = ids.shape[1]
+    if ids.shape[0] != T or wts.shape != ids.shape:
+        raise ValueError("topk_ids / topk_weights must be [T, topk]")
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    if workspace is None:
+        workspace = alloc_workspace(T, H, I, E, topk, fmt, dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if err is not None:
+        _need(err, "err", torch.int32, dev)
+    return dev, T, H, topk, out, workspace
+
+
+def fp8_forward(x, ids, wts, bank, limit: float, out=None, workspace=None, err=None, stream=None):
+    """Routed MoE FFN over an E4M3 bank with 128x128 block scales (moe_fp8_forward)."""
+    E, I, _ = bank.w_gate.shape
+    dev, T, H, topk, out, ws = _common(x, ids, wts, out, workspace, err, FMT_FP8, E, I)
+    for n in ("w_gate", "w_up", "w_down"):
+        _need(getattr(bank, n), n, torch.uint8, dev)
+    for n in ("s_gate", "s_up", "s_down"):
+        _need(getattr(bank, n), n, torch.float32, dev)
+    rc = load().moe_fp8_forward(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
+                                _ptr(bank.w_gate), _ptr(bank.s_gate), _ptr(bank.w_up),
+                                _ptr(bank.s_up), _ptr(bank.w_down), _ptr(bank.s_down),
+                                float(limit), _ptr(out), _ptr(ws), ws.numel(), _ptr(err),
+                                _stream(dev, stream))
+    _check("moe_fp8_forward", rc)
+    return out
+
+
+def nvfp4_forward(x, ids, wts, bank, limit: float, out=None, workspace=None, err=None, stream=None):
+    """Routed MoE FFN over an NVFP4 (W4A16) bank (moe_nvfp4_forward)."""
+    E, I, _ = bank.w_gate.shape
+    dev, T, H, topk, out, ws = _common(x, ids, wts, out, workspace, err, FMT_NVFP4, E, I)
+    for n in ("w_gate", "w_up", "w_down", "sf_gate", "sf_up", "sf_down"):
+        _need(getattr(bank, n), n, torch.uint8, dev)
+    rc = load().moe_nvfp4_forward(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
+                                  _ptr(bank.w_gate), _ptr(bank.sf_gate), float(bank.scale2_gate),
+                                  _ptr(bank.w_up), _ptr(bank.sf_up), float(bank.scale2_up),
+                                  _ptr(bank.w_down), _ptr(bank.sf_down), float(bank.scale2_down),
+                                  float(limit), _ptr(out), _ptr(ws), ws.numel(), _ptr(err),
+                                  _stream(dev, stream))
+    _check("moe_nvfp4_forward", rc)
+    return out
+
+
+def forward(x, ids, wts, bank, limit: float, **kw):
+    """Dispatch on the bank's format."""
+    if bank.fmt == "fp8":
+        return fp8_forward(x, ids, wts, bank, limit, **kw)
+    return nvfp4_forward(x, ids, wts, bank, limit, **kw)
+
+
+# ---- stages (T <= 8), for profiling and interleaving ----------------------------------------------
+
+def plan(ids, H, I, E, fmt, workspace, err=None, stream=None):
+    T, topk = ids.shape
+    rc = load().moe_plan(T, H, I, E, topk, fmt, _ptr(ids), _ptr(workspace), workspace.numel(),
+                         _ptr(err), _stream(ids.device, stream))
+    _check("moe_plan", rc)
+
+
+def gate_up(x, ids, bank, limit, workspace, err=None, stream=None):
+    T, H = x.shape
+    topk = ids.shape[1]
+    E, I, _ = bank.w_gate.shape
+    lib = load()
+    if bank.fmt == "fp8":
+        rc = lib.moe_fp8_gate_up(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(bank.w_gate),
+                                 _ptr(bank.s_gate), _ptr(bank.w_up), _ptr(bank.s_up), float(limit),
+                                 _ptr(workspace), workspace.numel(), _ptr(err),
+                                 _stream(x.device, stream))
+    else:
+        rc = lib.moe_nvfp4_gate_up(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(bank.w_gate),
+                                   _ptr(bank.sf_gate), float(bank.scale2_gate), _ptr(bank.w_up),
+                                   _ptr(bank.sf_up), float(bank.scale2_up), float(limit),
+                                   _ptr(workspace), workspace.numel(), _ptr(err),
+                                   _stream(x.device, stream))
+    _check("moe_*_gate_up", rc)
+
+
+def down_combine(ids, wts, bank, out, workspace, stream=None):
+    T, H = out.shape
+    topk = ids.shape[1]
+    E, I, _ = bank.w_gate.shape
+    lib = load()
+    if bank.fmt == "fp8":
+        rc = lib.moe_fp8_down_combine(T, H, I, E, topk, _ptr(ids), _ptr(wts), _ptr(bank.w_down),
+                                      _ptr(bank.s_down), _ptr(out), _ptr(workspace),
+                                      workspace.numel(), _stream(out.device, stream))
+    else:
+        rc = lib.moe_nvfp4_down_combine(T, H, I, E, topk, _ptr(ids), _ptr(wts), _ptr(bank.w_down),
+                                        _ptr(bank.sf_down), float(bank.scale2_down), _ptr(out),
+                                        _ptr(workspace), workspace.numel(),
+                                        _stream(out.device, stream))
+    _check("moe_*_down_combine", rc)
+
+
+def build_arch() -> str:
+    return load().moe_build_arch().decode()

@@ -1,0 +1,326 @@
+// C ABI of libmoe_ffn_gb300 (declared in include/moe_ffn.h): synchronous argument checks,
+// workspace carving, tier selection and the kernel launches. No allocation, no host sync.
+//
+// Tiers ("spark_model layers/glm5next_mlp/forward.rs", `gemm` / `forward_moe` tier policy:
+// M = 1 decode -> GEMV, M = 2..8 verify -> one weight sweep per union expert):
+//   T == 1      : gate_up (group = slot) -> down_combine.                          2 launches
+//   2 <= T <= 8 : route_plan (experts grouped, <= T columns each) -> gate_up -> down_combine.
+//   T > 8       : even row groups of <= 8 tokens ("forward.rs", `moe_row_groups`), each as above.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/moe_ffn.h"
+#include "kernels.cuh"
+
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxRowsPerSweep = 8;
+constexpr size_t kMaxSmem = 227 * 1024;
+
+bool shape_ok(int T, int H, int I, int E, int topk) {
+    return T >= 1 && topk >= 1 && topk <= kMaxTopk && H >= 128 && I >= 128 && H % 128 == 0 &&
+           I % 128 == 0 && E >= 1;
+}
+
+int rows_per_sweep(int T) { return T < kMaxRowsPerSweep ? T : kMaxRowsPerSweep; }
+
+// Largest number of columns a group can have for a sub-batch of `rows` tokens.
+int group_cap(int rows, int topk) {
+    const int p = rows * topk;
+    int cap = rows < kMaxCols ? rows : kMaxCols;
+    return cap < p ? cap : p;
+}
+
+int check_sizes(int T, int H, int I, int E, int topk) {
+    if (!shape_ok(T, H, I, E, topk)) return MOE_ERR_SHAPE;
+    const int rows = rows_per_sweep(T);
+    if (rows > 1 && E > kMaxPlanExperts) return MOE_ERR_UNSUPPORTED;
+    if (rows > 1 && route_plan_smem_bytes(E) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    const int cap = rows == 1 ? 1 : group_cap(rows, topk);
+    if (gate_up_smem_bytes(H, cap) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+struct Ws {
+    WsLayout L;
+    uint8_t* base;
+    template <class P> P* at(size_t off) const { return reinterpret_cast<P*>(base + off); }
+};
+
+int check_ws(void* ws, size_t bytes, int rows, int I, int E, int topk, Ws& out) {
+    if (ws == nullptr) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
+    out.L = ws_layout(rows, I, E, topk);
+    out.base = static_cast<uint8_t*>(ws);
+    if (bytes < out.L.total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+Groups groups_for(const Ws& w, const int32_t* ids, int rows, int topk, int E) {
+    Groups g{};
+    g.ids = ids;
+    g.topk = topk;
+    g.E = E;
+    if (rows > 1) {
+        g.count = w.at<int32_t>(w.L.group_count);
+        g.expert = w.at<int32_t>(w.L.group_expert);
+        g.start = w.at<int32_t>(w.L.group_start);
+        g.ncols = w.at<int32_t>(w.L.group_ncols);
+        g.sorted_pair = w.at<int32_t>(w.L.sorted_pair);
+    }
+    return g;
+}
+
+int cuda_status(cudaError_t st) { return st == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ---- the three stages for one sub-batch of rows <= 8 tokens --------------------------------
+
+int stage_plan(int rows, int E, int topk, const int32_t* ids, const Ws& w, int32_t* err,
+               cudaStream_t s) {
+    if (rows <= 1) return MOE_OK;
+    return cuda_status(launch_route_plan(
+        ids, rows * topk, E, group_cap(rows, topk), w.at<int32_t>(w.L.counts),
+        w.at<int32_t>(w.L.offsets), w.at<int32_t>(w.L.sorted_pair),
+        w.at<int32_t>(w.L.pair_to_sorted), w.at<int32_t>(w.L.group_count),
+        w.at<int32_t>(w.L.group_expert), w.at<int32_t>(w.L.group_start),
+        w.at<int32_t>(w.L.group_ncols), err, s));
+}
+
+template <int FMT>
+int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, const int32_t* ids,
+                  const uint8_t* wg, const float* sg, const uint8_t* sfg, float s2g,
+                  const uint8_t* wu, const float* su, const uint8_t* sfu, float s2u, float limit,
+                  const Ws& w, int32_t* err, cudaStream_t s) {
+    GateUpArgs a{};
+    a.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    a.H = H;
+    a.I = I;
+    a.wg = wg;
+    a.wu = wu;
+    a.sg = sg;
+    a.su = su;
+    a.sfg = sfg;
+    a.sfu = sfu;
+    a.s2g = s2g;
+    a.s2u = s2u;
+    a.limit = limit;
+    a.grp = groups_for(w, ids, rows, topk, E);
+    a.act = w.at<__half>(w.L.act);
+    a.act_scale = w.at<float>(w.L.act_scale);
+    a.err = err;
+    const int ngroups = rows * topk;     // implicit: topk slots; table: at most one per pair
+    const int cap = rows == 1 ? 1 : group_cap(rows, topk);
+    return cuda_status(launch_gate_up<FMT>(a, ngroups, cap, s));
+}
+
+template <int FMT>
+int stage_down(int rows, int H, int I, int E, int topk, const int32_t* ids, const float* wts,
+               const uint8_t* wd, const float* sd, const uint8_t* sfd, float s2d, uint16_t* out,
+               const Ws& w, cudaStream_t s) {
+    DownArgs a{};
+    a.T = rows;
+    a.H = H;
+    a.I = I;
+    a.topk = topk;
+    a.E = E;
+    a.ids = ids;
+    a.wts = wts;
+    a.wd = wd;
+    a.sd = sd;
+    a.sfd = sfd;
+    a.s2d = s2d;
+    a.grp = groups_for(w, ids, rows, topk, E);
+    a.act = w.at<__half>(w.L.act);
+    a.act_scale = w.at<float>(w.L.act_scale);
+    a.out = reinterpret_cast<__nv_bfloat16*>(out);
+    return cuda_status(launch_down_combine<FMT>(a, s));
+}
+
+struct Proj {
+    const uint8_t* w;
+    const float* s;       // FP8
+    const uint8_t* sf;    // NVFP4
+    float s2;
+};
+
+template <int FMT>
+int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32_t* ids,
+            const float* wts, Proj pg, Proj pu, Proj pd, float limit, uint16_t* out, void* ws,
+            size_t ws_bytes, int32_t* err, cudaStream_t s) {
+    int rc = check_sizes(T, H, I, E, topk);
+    if (rc) return rc;
+    const int rows_max = rows_per_sweep(T);
+    Ws w;
+    if ((rc = check_ws(ws, ws_bytes, rows_max, I, E, topk, w))) return rc;
+    // even split into ceil(T/8) groups, never a trailing group of one ("forward.rs",
+    // `moe_row_groups`); the workspace is rebuilt per group, in stream order.
+    const int ngroups = (T + kMaxRowsPerSweep - 1) / kMaxRowsPerSweep;
+    int start = 0;
+    for (int i = 0; i < ngroups; ++i) {
+        const int rows = (T - start + (ngroups - i) - 1) / (ngroups - i);
+        const int32_t* ids_g = ids + static_cast<size_t>(start) * topk;
+        const float* wts_g = wts + static_cast<size_t>(start) * topk;
+        const uint16_t* x_g = x + static_cast<size_t>(start) * H;
+        uint16_t* out_g = out + static_cast<size_t>(start) * H;
+        if ((rc = stage_plan(rows, E, topk, ids_g, w, err, s))) return rc;
+        if ((rc = stage_gate_up<FMT>(x_g, rows, H, I, E, topk, ids_g, pg.w, pg.s, pg.sf, pg.s2,
+                                     pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s)))
+            return rc;
+        if ((rc = stage_down<FMT>(rows, H, I, E, topk, ids_g, wts_g, pd.w, pd.s, pd.sf, pd.s2,
+                                  out_g, w, s)))
+            return rc;
+        start += rows;
+    }
+    return MOE_OK;
+}
+
+bool limit_ok(float limit) { return !std::isnan(limit) && limit > 0.0f; }
+
+// The kernels read weights and activations with 16-byte (FP8) / 8-byte (NVFP4) vector loads.
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+template <class... P>
+bool all_aligned(const P*... p) { return (aligned16(p) && ...); }
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(int T, int H, int I, int E, int topk, int fmt) {
+    if (fmt != MOE_FMT_FP8_E4M3_B128 && fmt != MOE_FMT_NVFP4) return 0;
+    if (check_sizes(T, H, I, E, topk) != MOE_OK) return 0;
+    return ws_layout(rows_per_sweep(T), I, E, topk).total;
+}
+
+int moe_route_permute(const int32_t* topk_ids, int T, int topk, int E, int32_t* counts,
+                      int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,
+                      int32_t* err, void* stream) {
+    if (!topk_ids || !counts || !offsets || !sorted_pair || !pair_to_sorted) return MOE_ERR_NULL;
+    if (T < 1 || topk < 1 || E < 1) return MOE_ERR_SHAPE;
+    if (E > kMaxPlanExperts || route_plan_smem_bytes(E) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    const long long P = static_cast<long long>(T) * topk;
+    if (P > (1LL << 30)) return MOE_ERR_SHAPE;
+    return cuda_status(launch_route_plan(topk_ids, static_cast<int>(P), E, 1, counts, offsets,
+                                         sorted_pair, pair_to_sorted, nullptr, nullptr, nullptr,
+                                         nullptr, err, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_fp8_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
+                    const int32_t* topk_ids, const float* topk_weights, const uint8_t* w_gate,
+                    const float* s_gate, const uint8_t* w_up, const float* s_up,
+                    const uint8_t* w_down, const float* s_down, float limit, uint16_t* out,
+                    void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!x || !topk_ids || !topk_weights || !w_gate || !s_gate || !w_up || !s_up || !w_down ||
+        !s_down || !out)
+        return MOE_ERR_NULL;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, w_down, out)) return MOE_ERR_ALIGN;
+    return forward<0>(x, T, H, I, E, topk, topk_ids, topk_weights, Proj{w_gate, s_gate, nullptr, 1.f},
+                      Proj{w_up, s_up, nullptr, 1.f}, Proj{w_down, s_down, nullptr, 1.f}, limit,
+                      out, workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream));
+}
+
+int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
+                      const int32_t* topk_ids, const float* topk_weights, const uint8_t* w_gate,
+                      const uint8_t* sf_gate, float scale2_gate, const uint8_t* w_up,
+                      const uint8_t* sf_up, float scale2_up, const uint8_t* w_down,
+                      const uint8_t* sf_down, float scale2_down, float limit, uint16_t* out,
+                      void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!x || !topk_ids || !topk_weights || !w_gate || !sf_gate || !w_up || !sf_up || !w_down ||
+        !sf_down || !out)
+        return MOE_ERR_NULL;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
+    if (!std::isfinite(scale2_gate) || !std::isfinite(scale2_up) || !std::isfinite(scale2_down))
+        return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, w_down, sf_gate, sf_up, sf_down, out)) return MOE_ERR_ALIGN;
+    return forward<1>(x, T, H, I, E, topk, topk_ids, topk_weights,
+                      Proj{w_gate, nullptr, sf_gate, scale2_gate},
+                      Proj{w_up, nullptr, sf_up, scale2_up},
+                      Proj{w_down, nullptr, sf_down, scale2_down}, limit, out, workspace,
+                      workspace_bytes, err, static_cast<cudaStream_t>(stream));
+}
+
+// ---- stage entry points (T <= 8: one sweep) -------------------------------------------------
+
+int moe_plan(int T, int H, int I, int E, int topk, int fmt, const int32_t* topk_ids,
+             void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!topk_ids) return MOE_ERR_NULL;
+    if (fmt != MOE_FMT_FP8_E4M3_B128 && fmt != MOE_FMT_NVFP4) return MOE_ERR_VALUE;
+    int rc = check_sizes(T, H, I, E, topk);
+    if (rc) return rc;
+    if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
+    Ws w;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    return stage_plan(T, E, topk, topk_ids, w, err, static_cast<cudaStream_t>(stream));
+}
+
+int moe_fp8_gate_up(const uint16_t* x, int T, int H, int I, int E, int topk,
+                    const int32_t* topk_ids, const uint8_t* w_gate, const float* s_gate,
+                    const uint8_t* w_up, const float* s_up, float limit, void* workspace,
+                    size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!x || !topk_ids || !w_gate || !s_gate || !w_up || !s_up) return MOE_ERR_NULL;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up)) return MOE_ERR_ALIGN;
+    int rc = check_sizes(T, H, I, E, topk);
+    if (rc) return rc;
+    if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
+    Ws w;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    return stage_gate_up<0>(x, T, H, I, E, topk, topk_ids, w_gate, s_gate, nullptr, 1.f, w_up,
+                            s_up, nullptr, 1.f, limit, w, err, static_cast<cudaStream_t>(stream));
+}
+
+int moe_fp8_down_combine(int T, int H, int I, int E, int topk, const int32_t* topk_ids,
+                         const float* topk_weights, const uint8_t* w_down, const float* s_down,
+                         uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!topk_ids || !topk_weights || !w_down || !s_down || !out) return MOE_ERR_NULL;
+    if (!all_aligned(w_down, out)) return MOE_ERR_ALIGN;
+    int rc = check_sizes(T, H, I, E, topk);
+    if (rc) return rc;
+    if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
+    Ws w;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    return stage_down<0>(T, H, I, E, topk, topk_ids, topk_weights, w_down, s_down, nullptr, 1.f,
+                         out, w, static_cast<cudaStream_t>(stream));
+}
+
+int moe_nvfp4_gate_up(const uint16_t* x, int T, int H, int I, int E, int topk,
+                      const int32_t* topk_ids, const uint8_t* w_gate, const uint8_t* sf_gate,
+                      float scale2_gate, const uint8_t* w_up, const uint8_t* sf_up,
+                      float scale2_up, float limit, void* workspace, size_t workspace_bytes,
+                      int32_t* err, void* stream) {
+    if (!x || !topk_ids || !w_gate || !sf_gate || !w_up || !sf_up) return MOE_ERR_NULL;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
+    if (!std::isfinite(scale2_gate) || !std::isfinite(scale2_up)) return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, sf_gate, sf_up)) return MOE_ERR_ALIGN;
+    int rc = check_sizes(T, H, I, E, topk);
+    if (rc) return rc;
+    if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
+    Ws w;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    return stage_gate_up<1>(x, T, H, I, E, topk, topk_ids, w_gate, nullptr, sf_gate, scale2_gate,
+                            w_up, nullptr, sf_up, scale2_up, limit, w, err,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int moe_nvfp4_down_combine(int T, int H, int I, int E, int topk, const int32_t* topk_ids,
+                           const float* topk_weights, const uint8_t* w_down,
+                           const uint8_t* sf_down, float scale2_down, uint16_t* out,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!topk_ids || !topk_weights || !w_down || !sf_down || !out) return MOE_ERR_NULL;
+    if (!std::isfinite(scale2_down)) return MOE_ERR_VALUE;
+    if (!all_aligned(w_down, sf_down, out)) return MOE_ERR_ALIGN;
+    int rc = check_sizes(T, H, I, E, topk);
+    if (rc) return rc;
+    if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
+    Ws w;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    return stage_down<1>(T, H, I, E, topk, topk_ids, topk_weights, w_down, nullptr, sf_down,
+                         scale2_down, out, w, static_cast<cudaStream_t>(stream));
+}
+
+const char* moe_build_arch(void) { return "sm_103a"; }
+
+}  // extern "C"

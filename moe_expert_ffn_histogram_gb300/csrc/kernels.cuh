@@ -1,0 +1,54 @@
+// Kernel argument blocks and launchers of libmoe_ffn_gb300 (internal to the library).
+#pragma once
+#include "moe_common.cuh"
+
+namespace moe {
+
+// Gate + up projections with the clamped SwiGLU fused (gate_up.cu).
+struct GateUpArgs {
+    const __nv_bfloat16* x;
+    int H, I;
+    const uint8_t* wg;
+    const uint8_t* wu;
+    const float* sg;      // FP8 block scales [E][I/128][H/128]
+    const float* su;
+    const uint8_t* sfg;   // NVFP4 scale bytes [E][I][H/16]
+    const uint8_t* sfu;
+    float s2g, s2u;       // NVFP4 scale_2
+    float limit;
+    Groups grp;
+    __half* act;          // [P][I] f16, range-scaled
+    float* act_scale;     // [P][I/64] inverse range scale
+    int32_t* err;
+};
+
+// Down projection fused with the slot-order combine (down_combine.cu).
+struct DownArgs {
+    int T, H, I, topk, E;
+    const int32_t* ids;     // [T][topk]
+    const float* wts;       // [T][topk]
+    const uint8_t* wd;
+    const float* sd;        // FP8 block scales [E][H/128][I/128]
+    const uint8_t* sfd;     // NVFP4 scale bytes [E][H][I/16]
+    float s2d;
+    Groups grp;
+    const __half* act;      // [P][I]
+    const float* act_scale; // [P][I/64]
+    __nv_bfloat16* out;     // [T][H]
+};
+
+// FMT: 0 = FP8 E4M3 with 128x128 block scales, 1 = NVFP4.
+template <int FMT> cudaError_t launch_gate_up(const GateUpArgs& a, int num_groups, int max_cols,
+                                              cudaStream_t stream);
+template <int FMT> cudaError_t launch_down_combine(const DownArgs& a, cudaStream_t stream);
+size_t gate_up_smem_bytes(int H, int max_cols);
+size_t down_smem_bytes(int T, int topk);
+
+// Route histogram / stable counting sort, optionally emitting expert groups (route_plan.cu).
+cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,
+                              int32_t* group_count, int32_t* group_expert, int32_t* group_start,
+                              int32_t* group_ncols, int32_t* err, cudaStream_t stream);
+size_t route_plan_smem_bytes(int E);
+
+}  // namespace moe

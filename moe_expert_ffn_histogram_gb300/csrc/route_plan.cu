@@ -1,0 +1,171 @@
+// Route histogram + stable counting sort of (token, slot) pairs by expert, and the expert groups
+// that the batched GEMV kernels sweep (each selected expert's weights read once per call).
+//
+// "spark_model layers/glm5next_mlp/forward.rs": the expert-sorted row order, expert_offsets[E+1]
+// and token_to_perm of `Glm5NextMlpWorkspace`, built by the `moe_sort_by_expert` step of
+// `forward_moe`; the "union" of a few rows' experts swept once each (doc comment of
+// `forward_moe`, `w4a16_gemv_moe_batchm`). Here both come from ONE single-block launch that
+// never returns to the host.
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exclusive scan of in[0..n) into out[0..n) by the whole block (blockDim.x == kPlanThreads).
+// Returns the total. in and out may alias. Uses scratch[33].
+__device__ int block_exclusive_scan(const int* in, int* out, int n, int* scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + kPlanThreads - 1) / kPlanThreads;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += in[i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = scratch[lane];
+        int wi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int u = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += u;
+        }
+        scratch[lane] = wi - v;
+        if (lane == 31) scratch[32] = wi;
+    }
+    __syncthreads();
+    int run = scratch[warp] + incl - local;
+    for (int i = lo; i < hi; ++i) {
+        const int v = in[i];
+        out[i] = run;
+        run += v;
+    }
+    const int total = scratch[32];
+    __syncthreads();
+    return total;
+}
+
+}  // namespace
+
+// One block of kPlanThreads threads. Dynamic shared memory: 3*E ints + 32*E bytes.
+// group_* may be null (plain permutation). cap = max columns per group (1..8).
+__global__ void __launch_bounds__(kPlanThreads, 1)
+route_plan_kernel(const int32_t* __restrict__ ids, int P, int E, int cap,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_to_sorted,
+                  int32_t* __restrict__ group_count, int32_t* __restrict__ group_expert,
+                  int32_t* __restrict__ group_start, int32_t* __restrict__ group_ncols,
+                  int32_t* __restrict__ err) {
+    extern __shared__ __align__(16) int smem_i[];
+    int* cnt = smem_i;                 // [E]
+    int* run = cnt + E;                // [E] offsets, then running cursor
+    int* tmp = run + E;                // [E] group counts / group bases
+    uint8_t* pre = reinterpret_cast<uint8_t*>(tmp + E);   // [32][E] per-warp counts of a round
+    __shared__ int scratch[33];
+    __shared__ int bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) bad = 0;
+    for (int e = tid; e < E; e += kPlanThreads) cnt[e] = 0;
+    for (int i = tid; i < 32 * E; i += kPlanThreads) pre[i] = 0;
+    __syncthreads();
+
+    // 1. histogram (integer atomics: the result does not depend on their order)
+    for (int p = tid; p < P; p += kPlanThreads) {
+        const int e = ids[p];
+        if (e >= 0 && e < E)
+            atomicAdd(&cnt[e], 1);
+        else if (e != -1)
+            bad = 1;
+    }
+    __syncthreads();
+
+    // 2. offsets
+    const int total = block_exclusive_scan(cnt, run, E, scratch);
+    for (int e = tid; e < E; e += kPlanThreads) {
+        counts[e] = cnt[e];
+        offsets[e] = run[e];
+    }
+    if (tid == 0) offsets[E] = total;
+
+    // 3. groups: ceil(count/cap) per expert, ascending expert, contiguous sorted pairs
+    if (group_count != nullptr) {
+        for (int e = tid; e < E; e += kPlanThreads) tmp[e] = (cnt[e] + cap - 1) / cap;
+        __syncthreads();
+        const int G = block_exclusive_scan(tmp, tmp, E, scratch);
+        for (int e = tid; e < E; e += kPlanThreads) {
+            const int c = cnt[e];
+            for (int j = 0, gi = tmp[e]; j * cap < c; ++j, ++gi) {
+                group_expert[gi] = e;
+                group_start[gi] = run[e] + j * cap;
+                group_ncols[gi] = min(cap, c - j * cap);
+            }
+        }
+        if (tid == 0) *group_count = G;
+    }
+    __syncthreads();
+
+    // 4. stable scatter, in rounds of kPlanThreads pairs (ascending pair index)
+    for (int base = 0; base < P; base += kPlanThreads) {
+        const int p = base + tid;
+        const int e = p < P ? ids[p] : -1;
+        const bool valid = p < P && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        const int rank = __popc(peers & lanemask_lt());
+        const bool leader = valid && rank == 0;
+        const int wc = __popc(peers);
+        if (leader) pre[warp * E + e] = static_cast<uint8_t>(wc);
+        __syncthreads();
+        if (valid) {
+            int s = 0;
+            for (int w = 0; w < warp; ++w) s += pre[w * E + e];
+            const int pos = run[e] + s + rank;
+            sorted_pair[pos] = p;
+            pair_to_sorted[p] = pos;
+        } else if (p < P) {
+            pair_to_sorted[p] = -1;
+        }
+        __syncthreads();
+        if (leader) {
+            atomicAdd(&run[e], wc);
+            pre[warp * E + e] = 0;
+        }
+        __syncthreads();
+    }
+    for (int s = total + tid; s < P; s += kPlanThreads) sorted_pair[s] = -1;
+    if (tid == 0 && bad && err != nullptr) atomicOr(err, 1);
+}
+
+size_t route_plan_smem_bytes(int E) { return static_cast<size_t>(E) * (3 * 4 + 32); }
+
+cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,
+                              int32_t* group_count, int32_t* group_expert, int32_t* group_start,
+                              int32_t* group_ncols, int32_t* err, cudaStream_t stream) {
+    const size_t smem = route_plan_smem_bytes(E);
+    if (smem > 48 * 1024) {
+        cudaError_t st = cudaFuncSetAttribute(route_plan_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(smem));
+        if (st != cudaSuccess) return st;
+    }
+    route_plan_kernel<<<1, kPlanThreads, smem, stream>>>(ids, P, E, cap, counts, offsets,
+                                                         sorted_pair, pair_to_sorted, group_count,
+                                                         group_expert, group_start, group_ncols,
+                                                         err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -227,24 +227,30 @@ def _normal_matrix(seed: int, expert: int, proj: str, n: int, k: int, device) ->
     return torch.randn(n, k, generator=g, device=device, dtype=torch.float32) * 0.02
 
 
-def make_fp8_bank(E: int, H: int, I: int, seed: int, device="cpu") -> Fp8Bank:
+def make_fp8_bank(E: int, H: int, I: int, seed: int, device="cpu", experts=None) -> Fp8Bank:
+    """Whole bank, or only the listed experts (in that order) of the same seeded bank."""
+    experts = list(range(E)) if experts is None else [int(e) for e in experts]
+    E = len(experts)
     wg = torch.empty(E, I, H, dtype=torch.uint8, device=device)
     wu = torch.empty(E, I, H, dtype=torch.uint8, device=device)
     wd = torch.empty(E, H, I, dtype=torch.uint8, device=device)
     sg = torch.empty(E, I // 128, H // 128, dtype=torch.float32, device=device)
     su = torch.empty_like(sg)
     sd = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=device)
-    for e in range(E):
+    for i, e in enumerate(experts):
         for proj, (wt, st, n, k) in {"gate": (wg, sg, I, H), "up": (wu, su, I, H),
                                      "down": (wd, sd, H, I)}.items():
             c, s = quantize_e4m3_blocks(_normal_matrix(seed, e, proj, n, k, device))
-            wt[e].copy_(c)
-            st[e].copy_(s)
+            wt[i].copy_(c)
+            st[i].copy_(s)
     return Fp8Bank(wg, sg, wu, su, wd, sd)
 
 
-def make_nvfp4_bank(E: int, H: int, I: int, seed: int, device="cpu") -> Nvfp4Bank:
+def make_nvfp4_bank(E: int, H: int, I: int, seed: int, device="cpu", experts=None) -> Nvfp4Bank:
+    """Whole bank, or only the listed experts of the same seeded bank (scale_2 is always taken
+    over the whole bank, as the full bank defines it)."""
     shapes = {"gate": (I, H), "up": (I, H), "down": (H, I)}
+    keep = list(range(E)) if experts is None else [int(e) for e in experts]
     scale2 = {}
     for proj, (n, k) in shapes.items():          # pass 1: bank-wide amax per projection
         amax = torch.zeros((), device=device)
@@ -254,12 +260,12 @@ def make_nvfp4_bank(E: int, H: int, I: int, seed: int, device="cpu") -> Nvfp4Ban
         scale2[proj] = float(np.float32(float(amax) / (E2M1_MAX * E4M3_MAX)))
     out = {}
     for proj, (n, k) in shapes.items():          # pass 2: regenerate and quantise
-        packed = torch.empty(E, n, k // 2, dtype=torch.uint8, device=device)
-        sf = torch.empty(E, n, k // 16, dtype=torch.uint8, device=device)
-        for e in range(E):
+        packed = torch.empty(len(keep), n, k // 2, dtype=torch.uint8, device=device)
+        sf = torch.empty(len(keep), n, k // 16, dtype=torch.uint8, device=device)
+        for i, e in enumerate(keep):
             p, s = quantize_nvfp4(_normal_matrix(seed, e, proj, n, k, device), scale2[proj])
-            packed[e].copy_(p)
-            sf[e].copy_(s)
+            packed[i].copy_(p)
+            sf[i].copy_(s)
         out[proj] = (packed, sf)
     return Nvfp4Bank(out["gate"][0], out["gate"][1], scale2["gate"],
                      out["up"][0], out["up"][1], scale2["up"],
@@ -295,28 +301,30 @@ def make_routes(kind: str, T: int, E: int, seed: int, topk: int = TOPK) -> torch
 
 
 def make_workload(name: str, device="cpu", bank=None, route_set: int = 0, T: Optional[int] = None,
-                  x_scale: float = 1.0) -> Workload:
+                  x_scale: float = 1.0, E: Optional[int] = None) -> Workload:
     """Build one named workload. ``bank`` may be passed to reuse an already generated bank;
-    ``route_set`` selects another seeded draw of routes/activations/weights for the same bank."""
+    ``route_set`` selects another seeded draw of routes/activations/weights for the same bank.
+    ``E`` restricts the bank to its first E experts (same bytes) and routes over those only."""
     c = CONFIGS[name]
     T = c["T"] if T is None else T
+    E = c["E"] if E is None else E
     seed = c["seed"] + 7919 * route_set
     if bank is None:
-        bank = make_bank(name, device)
+        bank = make_bank(name, device, experts=None if E == c["E"] else range(E))
     if c["x"] == "lcg":
         x = lcg_activations(T, c["H"], salt=route_set).to(device)
     else:
         x = normal_activations(T, c["H"], seed, device, scale=x_scale)
-    ids = make_routes(c["routes"], T, c["E"], seed).to(device)
+    ids = make_routes(c["routes"], T, E, seed).to(device)
     wts = softmax_route_weights(T, seed).to(device)
-    return Workload(name, c["fmt"], T, c["H"], c["I"], c["E"], TOPK, x, ids, wts, bank, LIMIT)
+    return Workload(name, c["fmt"], T, c["H"], c["I"], E, TOPK, x, ids, wts, bank, LIMIT)
 
 
-def make_bank(name: str, device="cpu"):
+def make_bank(name: str, device="cpu", experts=None):
     c = CONFIGS[name]
     if c["fmt"] == "fp8":
-        return make_fp8_bank(c["E"], c["H"], c["I"], c["bank_seed"], device)
-    return make_nvfp4_bank(c["E"], c["H"], c["I"], c["bank_seed"], device)
+        return make_fp8_bank(c["E"], c["H"], c["I"], c["bank_seed"], device, experts)
+    return make_nvfp4_bank(c["E"], c["H"], c["I"], c["bank_seed"], device, experts)
 
 
 def make_custom(fmt: str, T: int, H: int, I: int, E: int, seed: int, device="cpu",

@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle on the same seeded inputs.
+
+Integer outputs (route permutation) must match bit for bit; bf16 outputs must be within relative
+L2 <= 5e-3 and max abs <= 2e-2 * RMS(out) of the oracle's double result.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_ffn_histogram_gb300 import capi, inputs
+
+from helpers import bf16_to_f64, check_close, oracle_for
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_ffn_histogram_gb300 import _build
+    _build.build()
+    capi.load()
+
+
+def run(wl, **kw):
+    out = capi.forward(wl.x, wl.ids, wl.wts, wl.bank, wl.limit, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+# ---- route permutation: exact ---------------------------------------------------------------------
+
+def _check_permute(ids_np, E):
+    ids = torch.from_numpy(ids_np).to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r = capi.route_permute(ids, E, err=err)
+    torch.cuda.synchronize()
+    ref = oracle.route_permute(ids_np, E)
+    for k in ("counts", "offsets", "sorted_pair", "pair_to_sorted"):
+        assert np.array_equal(r[k].cpu().numpy(), ref[k]), k
+    assert int(err.item()) == ref["err"]
+
+
+@pytest.mark.parametrize("T,E,kind", [(1, 16, "uniform"), (3, 5, "uniform"), (8, 256, "low64"),
+                                      (37, 64, "uniform"), (1000, 256, "zipf"),
+                                      (4096, 256, "zipf"), (129, 4096, "uniform")])
+def test_route_permute_exact(T, E, kind):
+    topk = min(8, E)
+    ids = inputs.sampled_routes(T, E, kind, seed=T * 31 + E, topk=topk).numpy()
+    rng = np.random.default_rng(T)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    _check_permute(ids.astype(np.int32), E)
+
+
+def test_route_permute_skew_and_degenerate():
+    _check_permute(np.full((300, 8), 7, np.int32), 16)                  # every pair on one expert
+    _check_permute(np.full((5, 8), -1, np.int32), 16)                   # nothing routed
+    bad = np.zeros((4, 8), np.int32)
+    bad[1, 3] = 99
+    bad[2, 0] = -7
+    _check_permute(bad, 16)                                             # out-of-range ids flagged
+
+
+# ---- FFN parity on small shapes (several tiles, ragged T) -------------------------------------------
+
+SMALL = [
+    ("fp8", 1, 256, 128, 16), ("fp8", 1, 384, 256, 12), ("fp8", 2, 256, 384, 9),
+    ("fp8", 3, 640, 256, 12), ("fp8", 5, 256, 128, 20), ("fp8", 8, 384, 256, 24),
+    ("fp8", 11, 256, 256, 16), ("fp8", 20, 128, 128, 40),
+    ("nvfp4", 1, 256, 128, 16), ("nvfp4", 1, 512, 384, 10), ("nvfp4", 3, 384, 256, 12),
+    ("nvfp4", 8, 256, 256, 24), ("nvfp4", 13, 256, 128, 16),
+]
+
+
+@pytest.mark.parametrize("fmt,T,H,I,E", SMALL)
+def test_small_parity(fmt, T, H, I, E):
+    wl = inputs.make_custom(fmt, T, H, I, E, seed=100 + T + H + E, device=DEV)
+    out = run(wl)
+    ref = oracle_for(wl)["out"]
+    check_close(bf16_to_f64(out), ref, f"{fmt} T={T} H={H} I={I} E={E}")
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_topk_below_eight(fmt):
+    wl = inputs.make_custom(fmt, 4, 256, 128, 6, seed=9, device=DEV, topk=3)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"{fmt} topk=3")
+
+
+def test_tiny_fp8_decode_config():
+    wl = inputs.make_workload("tiny_fp8_decode", device=DEV)
+    assert wl.ids.tolist() == [[0, 2, 4, 6, 8, 10, 12, 14]]
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], "tiny_fp8_decode")
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_clamp_stress(fmt):
+    """Activations x40: many gates above the limit and ups outside +-limit."""
+    wl = inputs.make_custom(fmt, 3, 512, 256, 12, seed=77, device=DEV, x_scale=40.0)
+    res = oracle_for(wl)
+    check_close(bf16_to_f64(run(wl)), res["out"], f"{fmt} clamp stress")
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_no_limit(fmt):
+    wl = inputs.make_custom(fmt, 2, 256, 256, 10, seed=78, device=DEV, x_scale=20.0,
+                            limit=float("inf"))
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"{fmt} limit=inf")
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_unfilled_and_bad_ids(T):
+    wl = inputs.make_custom("fp8", T, 256, 128, 16, seed=5, device=DEV)
+    ids = wl.ids.clone()
+    ids[0, 1] = -1
+    ids[0, 5] = 16          # == E: out of range
+    ids[T - 1, 7] = -9
+    wl.ids = ids
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(wl, err=err)
+    assert int(err.item()) & capi.ERRBIT_BAD_ID
+    res = oracle_for(wl)
+    assert res["err"] & 1
+    check_close(bf16_to_f64(out), res["out"], "bad ids")
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_nothing_routed_gives_zero(T):
+    wl = inputs.make_custom("fp8", T, 256, 128, 16, seed=6, device=DEV)
+    wl.ids = torch.full_like(wl.ids, -1)
+    out = torch.full((T, 256), float("nan"), dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    run(wl, out=out, err=err)
+    assert torch.equal(out.float(), torch.zeros_like(out.float()))
+    assert int(err.item()) == 0
+
+
+def test_duplicate_ids_in_a_token_are_summed():
+    wl = inputs.make_custom("fp8", 3, 256, 128, 16, seed=7, device=DEV)
+    ids = wl.ids.clone()
+    ids[0, :] = 3           # all 8 slots of token 0 on expert 3
+    ids[1, 2] = ids[1, 5]
+    wl.ids = ids
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], "duplicates")
+    wl1 = inputs.make_custom("nvfp4", 1, 256, 128, 16, seed=8, device=DEV)
+    wl1.ids = torch.full_like(wl1.ids, 2)
+    check_close(bf16_to_f64(run(wl1)), oracle_for(wl1)["out"], "duplicates T=1")
+
+
+# ---- determinism, guards, stages -----------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,T", [("fp8", 1), ("fp8", 6), ("nvfp4", 1), ("nvfp4", 5)])
+def test_bitwise_repeatable(fmt, T):
+    wl = inputs.make_custom(fmt, T, 384, 256, 16, seed=10 + T, device=DEV)
+    a = run(wl).clone()
+    for _ in range(3):
+        assert torch.equal(run(wl).view(torch.int16), a.view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt,T", [("fp8", 1), ("fp8", 7), ("nvfp4", 2)])
+def test_output_tail_sentinel_untouched(fmt, T):
+    wl = inputs.make_custom(fmt, T, 256, 128, 16, seed=11, device=DEV)
+    H = wl.H
+    buf = torch.full((T * H + 17,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    sentinel = buf[T * H:].clone()
+    out = buf[: T * H].view(T, H)
+    run(wl, out=out)
+    assert torch.equal(buf[T * H:].view(torch.int16), sentinel.view(torch.int16))
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("fmt,T", [("fp8", 1), ("fp8", 5), ("nvfp4", 1), ("nvfp4", 8)])
+def test_stages_equal_forward(fmt, T):
+    wl = inputs.make_custom(fmt, T, 256, 256, 16, seed=12, device=DEV)
+    ref = run(wl).clone()
+    f = capi.FMT_FP8 if fmt == "fp8" else capi.FMT_NVFP4
+    ws = capi.alloc_workspace(T, wl.H, wl.I, wl.E, wl.topk, f, DEV)
+    out = torch.empty_like(ref)
+    capi.plan(wl.ids, wl.H, wl.I, wl.E, f, ws)
+    capi.gate_up(wl.x, wl.ids, wl.bank, wl.limit, ws)
+    capi.down_combine(wl.ids, wl.wts, wl.bank, out, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_workspace_too_small_is_rejected_on_device_path():
+    wl = inputs.make_custom("fp8", 2, 256, 128, 16, seed=13, device=DEV)
+    n = capi.workspace_bytes(2, 256, 128, 16, 8, capi.FMT_FP8)
+    ws = torch.empty(n - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(capi.MoeError) as e:
+        run(wl, workspace=ws)
+    assert e.value.code == -3
+
+
+def test_stream_ordering_on_a_side_stream():
+    wl = inputs.make_custom("fp8", 4, 256, 128, 16, seed=14, device=DEV)
+    ref = run(wl).clone()
+    s = torch.cuda.Stream(device=DEV)
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        out = capi.forward(wl.x, wl.ids, wl.wts, wl.bank, wl.limit)
+    s.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+# ---- the named workloads at full size ---------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def fp8_bank():
+    return inputs.make_bank("fp8_decode", DEV)
+
+
+def test_fp8_decode_full_size(fp8_bank):
+    for rs in range(2):
+        wl = inputs.make_workload("fp8_decode", device=DEV, bank=fp8_bank, route_set=rs)
+        check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"fp8_decode set {rs}")
+
+
+def test_fp8_decode_clamp_stress_full_size(fp8_bank):
+    wl = inputs.make_workload("fp8_decode", device=DEV, bank=fp8_bank, x_scale=8.0)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], "fp8_decode x8")
+
+
+def test_fp8_batchm_full_size(fp8_bank):
+    wl = inputs.make_workload("fp8_batchm", device=DEV, bank=fp8_bank)
+    ids = wl.ids.cpu().numpy()
+    assert ids.max() < 64 and len(set(ids.reshape(-1).tolist())) < 64
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], "fp8_batchm")
+
+
+def test_fp8_prefill_full_size_sampled(fp8_bank):
+    wl = inputs.make_workload("fp8_prefill", device=DEV, bank=fp8_bank)
+    out = run(wl)
+    toks = [0, 1, 777, 2048, 3333, 4095]
+    res = oracle_for(wl, tokens=toks)
+    check_close(bf16_to_f64(out[toks]), res["out"], "fp8_prefill sampled")
+    # route permutation at the full prefill size, exactly
+    _check_permute(wl.ids.cpu().numpy(), wl.E)
+
+
+def test_nvfp4_decode_full_size():
+    bank = inputs.make_bank("nvfp4_decode", DEV)
+    for rs in range(2):
+        wl = inputs.make_workload("nvfp4_decode", device=DEV, bank=bank, route_set=rs)
+        check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"nvfp4_decode set {rs}")

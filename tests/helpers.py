@@ -36,17 +36,15 @@ def oracle_for(wl, tokens=None, ids=None, x_bits=None, limit=None, nthreads=0):
     rows = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
     used = sorted({int(e) for e in ids[rows].reshape(-1) if 0 <= e < wl.E})
     remap = {e: i for i, e in enumerate(used)}
-    sub_ids = ids.copy()
-    for (t, k), e in np.ndenumerate(ids):
-        if 0 <= e < wl.E:
-            sub_ids[t, k] = remap[int(e)]
-        elif e != -1:
-            sub_ids[t, k] = len(used) + 1 + 10_000     # stays out of range for the sub-bank
+    sub_ids = np.full_like(ids, -1)          # rows outside `tokens` are never read
+    for t in rows:
+        for k, e in enumerate(ids[t]):
+            if 0 <= e < wl.E:
+                sub_ids[t, k] = remap[int(e)]
+            elif e != -1:
+                sub_ids[t, k] = len(used) + 10_000     # stays out of range for the sub-bank
     if not used:
         used = [0]
     bank = wl.bank.numpy(torch.tensor(used, dtype=torch.long))
-    E_sub = len(used)
-    # ids out of the sub-bank range must still count as "bad" exactly when they were bad
-    sub_ids[(ids >= wl.E) | (ids < -1)] = E_sub + 10_000
     fn = oracle.moe_fp8 if wl.fmt == "fp8" else oracle.moe_nvfp4
     return fn(xb, sub_ids, wts, bank, limit, tokens=tokens, nthreads=nthreads)

@@ -181,6 +181,33 @@ MOE_API int moe_nvfp4_down_combine(int T, int H, int I, int E, int topk, const i
                            const uint8_t* sf_down, float scale2_down, uint16_t* out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * moe_fp8_forward_noalloc - moe_fp8_forward for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point. It exists for callers that cannot call
+ * cudaMalloc or pass a workspace: for example a plugin that only receives input and output
+ * pointers through a fixed interface, or a latency-critical loop that forbids device allocation
+ * because cudaMalloc/cudaFree can implicitly synchronise the device. Arguments are those of
+ * moe_fp8_forward without the workspace; the caller still passes every input and the output.
+ *
+ * Scratch: a file-scope device array of MOE_NOALLOC_SCRATCH_BYTES inside the library, present on
+ * every GPU that loads the library until the process exits. Calls whose
+ * moe_workspace_bytes(T, H, I, E, topk, MOE_FMT_FP8_E4M3_B128) exceeds it return
+ * MOE_ERR_WORKSPACE with nothing enqueued (e.g. T <= 8, I = 2048, E = 256 needs about 270 KB).
+ * All calls on a device share the array and it keeps the last call's contents; nothing in it
+ * needs to start at zero. Calls that overlap on the GPU race on it: serialise them.
+ * The first call on each device (with that device current) looks up the array's device address
+ * with cudaGetSymbolAddress, which may load the library's kernels; make it before any stream
+ * capture. No cudaMalloc, cudaFree or allocating library routine is ever called.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+MOE_API int moe_fp8_forward_noalloc(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                    const int32_t* topk_ids, const float* topk_weights,
+                                    const uint8_t* w_gate, const float* s_gate,
+                                    const uint8_t* w_up, const float* s_up,
+                                    const uint8_t* w_down, const float* s_down, float limit,
+                                    uint16_t* out, int32_t* err, void* stream);
+
 /* Library build identification: the compiled CUDA architecture string (e.g. "sm_103a"). */
 MOE_API const char* moe_build_arch(void);
 

@@ -24,7 +24,7 @@ ERRBIT_BAD_ID = 1
 
 EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_nvfp4_forward",
             "moe_plan", "moe_fp8_gate_up", "moe_fp8_down_combine", "moe_nvfp4_gate_up",
-            "moe_nvfp4_down_combine", "moe_build_arch")
+            "moe_nvfp4_down_combine", "moe_build_arch", "moe_fp8_forward_noalloc")
 
 _lib = None
 

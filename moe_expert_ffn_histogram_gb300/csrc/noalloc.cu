@@ -1,0 +1,78 @@
+// moe_fp8_forward_noalloc: the FP8 routed-MoE forward for callers that cannot allocate device
+// memory.
+//
+// Some callers of this library cannot call cudaMalloc or hand it a workspace: a plugin that only
+// receives input and output pointers through a fixed interface (no workspace argument, no access
+// to the host framework's allocator), or a latency-critical serving loop that forbids device
+// allocation because cudaMalloc/cudaFree can implicitly synchronise the device and stall every
+// stream. This entry point gives them the forward without a workspace argument: its scratch is a
+// file-scope device array of fixed size, so nothing is allocated at call time.
+//
+// Contract:
+//   * The scratch is MOE_NOALLOC_SCRATCH_BYTES (1 MiB) in every GPU's memory that loads the library,
+//     held until the process exits. Calls whose moe_workspace_bytes() exceeds it are rejected
+//     with MOE_ERR_WORKSPACE before anything is enqueued.
+//   * All calls on one device share that array, and it keeps the last call's contents. Nothing in
+//     it needs to start at zero: every call writes each region before reading it. Calls that
+//     overlap on the GPU (e.g. on two streams at once) race on the array; serialise them (one
+//     stream, or events).
+//   * The first call on each device, with that device current, looks up the array's device
+//     address with cudaGetSymbolAddress (which may load the library's kernels on that device).
+//     Make that first call before any stream capture.
+//   * No cudaMalloc, cudaFree or allocating library routine is called.
+// The pages have no counterpart to this entry point.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/moe_ffn.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_setup_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (host code must not use the
+// array's name as a pointer: on the host it is only a stand-in for the symbol).
+int scratch_on_current_device(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t st = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (st != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_fp8_forward_noalloc(const uint16_t* x, int T, int H, int I, int E, int topk,
+                            const int32_t* topk_ids, const float* topk_weights,
+                            const uint8_t* w_gate, const float* s_gate, const uint8_t* w_up,
+                            const float* s_up, const uint8_t* w_down, const float* s_down,
+                            float limit, uint16_t* out, int32_t* err, void* stream) {
+    const size_t need = moe_workspace_bytes(T, H, I, E, topk, MOE_FMT_FP8_E4M3_B128);
+    if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+    if (need == 0)   // invalid sizes: report exactly what moe_fp8_forward reports, enqueue nothing
+        return moe_fp8_forward(x, T, H, I, E, topk, topk_ids, topk_weights, w_gate, s_gate, w_up,
+                               s_up, w_down, s_down, limit, out, nullptr, 0, err, stream);
+    void* scratch = nullptr;
+    const int rc = scratch_on_current_device(&scratch);
+    if (rc != MOE_OK) return rc;
+    return moe_fp8_forward(x, T, H, I, E, topk, topk_ids, topk_weights, w_gate, s_gate, w_up, s_up,
+                           w_down, s_down, limit, out, scratch, kNoAllocScratchBytes, err, stream);
+}
+
+}  // extern "C"

@@ -64,6 +64,9 @@ typedef enum {
 } moe_format;
 
 #define MOE_ERRBIT_BAD_ID 1
+/* A grid-wide barrier of the fused forward gave up after ~2 s (possible only if the GPU could not
+ * keep all CTAs of the cooperative launch resident); the output of that call is incomplete. */
+#define MOE_ERRBIT_BARRIER 2
 
 /*
  * moe_workspace_bytes - device scratch needed by moe_fp8_forward / moe_nvfp4_forward for a call
@@ -145,10 +148,11 @@ MOE_API int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int
                       int32_t* err, void* stream);
 
 /*
- * Stage entry points. moe_*_forward is exactly moe_plan (when T > 1), then moe_*_gate_up, then
- * moe_*_down_combine, on one stream. They are exported so that a caller (or a profiler) can
- * time or interleave the stages; each takes the same arguments as the forward call it belongs
- * to and the same workspace, and must be called in that order for one forward.
+ * Stage entry points. moe_plan, then moe_*_gate_up, then moe_*_down_combine (on one stream, same
+ * workspace, same arguments as the forward they stand for) compute exactly the bits of
+ * moe_*_forward for T <= 8, as three separate kernels; moe_*_forward runs the same work items in
+ * one fused cooperative launch. They are exported so that a caller (or a profiler) can time or
+ * interleave the stages.
  *
  * moe_plan            - groups the routed (token, slot) pairs by expert into the workspace
  *                       (one launch; a no-op for T == 1, where slot k is group k).

@@ -47,15 +47,18 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_path: str = None) -> str:
+    """Build the library (or, with out_path and extra_flags, a variant build of it elsewhere)."""
+    target = out_path or LIB_PATH
+    if not force and out_path is None and up_to_date():
         return LIB_PATH
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    objs = []
+    bdir = BUILD_DIR if out_path is None else os.path.join(
+        BUILD_DIR, os.path.splitext(os.path.basename(out_path))[0])
+    os.makedirs(bdir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH_FLAGS, *NVCC_FLAGS, *extra_flags, "-I", os.path.join(ROOT, "include"),
                "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -68,13 +71,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = target + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, target)
+    return target
 
 
 if __name__ == "__main__":

@@ -2,10 +2,15 @@
 // workspace carving, tier selection and the kernel launches. No allocation, no host sync.
 //
 // Tiers ("spark_model layers/glm5next_mlp/forward.rs", `gemm` / `forward_moe` tier policy:
-// M = 1 decode -> GEMV, M = 2..8 verify -> one weight sweep per union expert):
-//   T == 1      : gate_up (group = slot) -> down_combine.                          2 launches
-//   2 <= T <= 8 : route_plan (experts grouped, <= T columns each) -> gate_up -> down_combine.
+// M = 1 decode -> GEMV, M = 2..8 verify -> one weight sweep per union expert), chosen by
+// measurement on GB300:
+//   T == 1      : gate_up kernel (group = slot) -> down_combine kernel, the latter launched as a
+//                 programmatic dependent that starts its weight stream while gate_up drains.
+//   2 <= T <= 8 : one fused cooperative launch (fused.cu): in-kernel expert grouping, gate/up +
+//                 SwiGLU, grid barrier, down + slot-order combine (after a 4-byte barrier memset).
 //   T > 8       : even row groups of <= 8 tokens ("forward.rs", `moe_row_groups`), each as above.
+// The stage entry points (moe_plan, moe_*_gate_up, moe_*_down_combine) run the same work items
+// as separate kernels and give the same bits.
 #include <cmath>
 #include <cstdint>
 
@@ -14,6 +19,13 @@
 
 
 using namespace moe;
+
+#ifndef MOE_FORWARD_FUSED
+#define MOE_FORWARD_FUSED 1
+#endif
+#ifndef MOE_FORCE_FUSED
+#define MOE_FORCE_FUSED 0
+#endif
 
 namespace {
 
@@ -41,6 +53,8 @@ int check_sizes(int T, int H, int I, int E, int topk) {
     if (rows > 1 && route_plan_smem_bytes(E) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
     const int cap = rows == 1 ? 1 : group_cap(rows, topk);
     if (gate_up_smem_bytes(H, cap) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    if (down_smem_bytes(rows, topk) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    if (fused_smem_bytes(H, rows, topk, cap) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -139,6 +153,54 @@ int stage_down(int rows, int H, int I, int E, int topk, const int32_t* ids, cons
     return cuda_status(launch_down_combine<FMT>(a, s));
 }
 
+// The whole forward of one sub-batch as one fused cooperative launch (grouping done in-kernel).
+template <int FMT>
+int stage_fused(const uint16_t* x, int rows, int H, int I, int E, int topk, const int32_t* ids,
+                const float* wts, const uint8_t* wg, const float* sg, const uint8_t* sfg, float s2g,
+                const uint8_t* wu, const float* su, const uint8_t* sfu, float s2u,
+                const uint8_t* wd, const float* sd, const uint8_t* sfd, float s2d, float limit,
+                uint16_t* out, const Ws& w, int32_t* err, cudaStream_t s) {
+    Groups grp{};
+    grp.ids = ids;
+    grp.topk = topk;
+    grp.E = E;
+    GateUpArgs ga{};
+    ga.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    ga.H = H;
+    ga.I = I;
+    ga.wg = wg;
+    ga.wu = wu;
+    ga.sg = sg;
+    ga.su = su;
+    ga.sfg = sfg;
+    ga.sfu = sfu;
+    ga.s2g = s2g;
+    ga.s2u = s2u;
+    ga.limit = limit;
+    ga.grp = grp;
+    ga.act = w.at<__half>(w.L.act);
+    ga.act_scale = w.at<float>(w.L.act_scale);
+    ga.err = err;
+    DownArgs da{};
+    da.T = rows;
+    da.H = H;
+    da.I = I;
+    da.topk = topk;
+    da.E = E;
+    da.ids = ids;
+    da.wts = wts;
+    da.wd = wd;
+    da.sd = sd;
+    da.sfd = sfd;
+    da.s2d = s2d;
+    da.grp = grp;
+    da.act = ga.act;
+    da.act_scale = ga.act_scale;
+    da.out = reinterpret_cast<__nv_bfloat16*>(out);
+    const int cap = rows == 1 ? 1 : group_cap(rows, topk);
+    return cuda_status(launch_fused_forward<FMT>(ga, da, w.at<unsigned>(w.L.barrier), rows, cap, s));
+}
+
 struct Proj {
     const uint8_t* w;
     const float* s;       // FP8
@@ -165,13 +227,20 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
         const float* wts_g = wts + static_cast<size_t>(start) * topk;
         const uint16_t* x_g = x + static_cast<size_t>(start) * H;
         uint16_t* out_g = out + static_cast<size_t>(start) * H;
-        if ((rc = stage_plan(rows, E, topk, ids_g, w, err, s))) return rc;
-        if ((rc = stage_gate_up<FMT>(x_g, rows, H, I, E, topk, ids_g, pg.w, pg.s, pg.sf, pg.s2,
-                                     pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s)))
-            return rc;
-        if ((rc = stage_down<FMT>(rows, H, I, E, topk, ids_g, wts_g, pd.w, pd.s, pd.sf, pd.s2,
-                                  out_g, w, s)))
-            return rc;
+        if (MOE_FORWARD_FUSED && (rows > 1 || MOE_FORCE_FUSED)) {
+            if ((rc = stage_fused<FMT>(x_g, rows, H, I, E, topk, ids_g, wts_g, pg.w, pg.s, pg.sf,
+                                       pg.s2, pu.w, pu.s, pu.sf, pu.s2, pd.w, pd.s, pd.sf, pd.s2,
+                                       limit, out_g, w, err, s)))
+                return rc;
+        } else {
+            if ((rc = stage_plan(rows, E, topk, ids_g, w, err, s))) return rc;
+            if ((rc = stage_gate_up<FMT>(x_g, rows, H, I, E, topk, ids_g, pg.w, pg.s, pg.sf, pg.s2,
+                                         pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s)))
+                return rc;
+            if ((rc = stage_down<FMT>(rows, H, I, E, topk, ids_g, wts_g, pd.w, pd.s, pd.sf, pd.s2,
+                                      out_g, w, s)))
+                return rc;
+        }
         start += rows;
     }
     return MOE_OK;

@@ -44,6 +44,13 @@ template <int FMT> cudaError_t launch_down_combine(const DownArgs& a, cudaStream
 size_t gate_up_smem_bytes(int H, int max_cols);
 size_t down_smem_bytes(int T, int topk);
 
+// The whole forward of one sub-batch in one cooperative launch (fused.cu); `barrier` is a
+// workspace word, zeroed by the launcher with a memset on `stream`.
+template <int FMT> cudaError_t launch_fused_forward(const GateUpArgs& ga, const DownArgs& da,
+                                                    unsigned* barrier, int rows, int cap,
+                                                    cudaStream_t stream);
+size_t fused_smem_bytes(int H, int rows, int topk, int cap);
+
 // Route histogram / stable counting sort, optionally emitting expert groups (route_plan.cu).
 cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,
                               int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,

@@ -25,6 +25,7 @@ constexpr int kMaxPlanExperts = 4096;
 // ---- workspace -------------------------------------------------------------------------------
 
 struct WsLayout {
+    size_t barrier;
     size_t group_count, group_expert, group_start, group_ncols;
     size_t counts, offsets, sorted_pair, pair_to_sorted;
     size_t act, act_scale;
@@ -39,6 +40,7 @@ __host__ __device__ inline WsLayout ws_layout(int rows, int I, int E, int topk) 
     WsLayout L{};
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    L.barrier = take(16);
     L.group_count = take(16);
     L.group_expert = take(P * 4);
     L.group_start = take(P * 4);
@@ -130,6 +132,41 @@ __device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
     asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
+
+// Fire-and-forget bulk prefetch of [p, p + bytes) into L2 (bytes a multiple of 16, p 16-aligned):
+// no registers, no shared memory, no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start launching, and (in that
+// kernel) wait until every grid it depends on has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Asynchronous global -> shared copies (per-thread, completion tracked with commit/wait groups).
+// 16-byte copies bypass L1 (.cg); 8- and 4-byte copies only exist in the .ca form.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 
 // ---- power-of-two range scales -----------------------------------------------------------------
 

@@ -76,7 +76,7 @@ route_plan_kernel(const int32_t* __restrict__ ids, int P, int E, int cap,
     __shared__ int scratch[33];
     __shared__ int bad;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) bad = 0;
     for (int e = tid; e < E; e += kPlanThreads) cnt[e] = 0;
     for (int i = tid; i < 32 * E; i += kPlanThreads) pre[i] = 0;

@@ -12,7 +12,7 @@ namespace moe {
 size_t down_smem_bytes(int T, int topk) { return down_item_smem(T, topk); }
 
 template <int FMT>
-__global__ void __launch_bounds__(kItemThreads, kMinBlocks) down_combine_kernel(const DownArgs a) {
+__global__ void __launch_bounds__(kItemThreads, kDownMinBlocks) down_combine_kernel(const DownArgs a) {
     extern __shared__ __align__(16) float ys[];     // [P][16]
     __shared__ GroupList gl;
     load_group_list(a.grp, gl);

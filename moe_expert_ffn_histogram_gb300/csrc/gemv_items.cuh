@@ -27,7 +27,7 @@ constexpr int kMaxPairs = kMaxTopk * kMaxCols;   // pairs of one sub-batch (<= 8
 #define MOE_GU_BATCH 4
 #endif
 #ifndef MOE_GU_BATCH_FP4
-#define MOE_GU_BATCH_FP4 8
+#define MOE_GU_BATCH_FP4 4
 #endif
 #ifndef MOE_DN_BATCH
 #define MOE_DN_BATCH 4
@@ -35,10 +35,14 @@ constexpr int kMaxPairs = kMaxTopk * kMaxCols;   // pairs of one sub-batch (<= 8
 #ifndef MOE_MIN_BLOCKS
 #define MOE_MIN_BLOCKS 2
 #endif
+#ifndef MOE_DN_MIN_BLOCKS
+#define MOE_DN_MIN_BLOCKS 3
+#endif
 constexpr int kStagesFp8 = MOE_GU_BATCH;      // 128-wide K blocks per load batch (128 B per row each)
-constexpr int kStagesFp4 = MOE_GU_BATCH_FP4;  // 64-wide K segments per load batch (32 B per row each)
+constexpr int kStagesFp4 = MOE_GU_BATCH_FP4;  // 128-wide K super-segments per batch (64 B per row each)
 constexpr int kDownBatch = MOE_DN_BATCH;      // 64-wide K segments per down load batch
 constexpr int kMinBlocks = MOE_MIN_BLOCKS;    // CTAs per SM the register budget is sized for
+constexpr int kDownMinBlocks = MOE_DN_MIN_BLOCKS;   // the same, for the down stage kernel
 
 // One routed group as a CTA sees it: its expert and the routed pairs (t*topk + k) it serves.
 struct GroupView {
@@ -204,49 +208,66 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
             }
         }
     } else {
+        // NVFP4: the per-16 scale bytes fold into A, so nothing needs the 64-wide K interleave of
+        // the FP8 path. A lane streams 16 bytes (32 codes) of each row per 128-wide super-segment
+        // t: elements 128t + 32c .. +31, i.e. MMA step i (0..7) takes elements 4i..4i+3 of those;
+        // B is read at the same physical positions. The row's 8 scale bytes of a super-segment
+        // come in one 8-byte load shared by the row's 4 lanes; lane c uses bytes 2c and 2c+1.
         const size_t row = static_cast<size_t>(e) * I + n;
-        const uint8_t* pg = a.wg + row * (H / 2) + c * 8;
-        const uint8_t* pu = a.wu + row * (H / 2) + c * 8;
-        const uint8_t* fgp = a.sfg + row * (H / 16) + c;
-        const uint8_t* fup = a.sfu + row * (H / 16) + c;
-        const int nseg = H / 64;
-        for (int s0 = 0; s0 < nseg; s0 += kStagesFp4) {
-            uint2 qg[kStagesFp4], qu[kStagesFp4];
-            uint32_t fg[kStagesFp4], fu[kStagesFp4];
+        const uint8_t* pg = a.wg + row * (H / 2) + c * 16;
+        const uint8_t* pu = a.wu + row * (H / 2) + c * 16;
+        const uint8_t* fgp = a.sfg + row * (H / 16);
+        const uint8_t* fup = a.sfu + row * (H / 16);
+        const __half* xb4 = xs + static_cast<size_t>(has_b ? g : 0) * H + c * 32;
+        const int nsup = H / 128;
+        const int sf_shift = 16 * (c & 1);
+        for (int t0 = 0; t0 < nsup; t0 += kStagesFp4) {
+            uint4 qg[kStagesFp4], qu[kStagesFp4];
+            uint2 fg[kStagesFp4], fu[kStagesFp4];
 #pragma unroll
             for (int s = 0; s < kStagesFp4; ++s) {
-                if (s0 + s < nseg) {
-                    qg[s] = ld_stream_v2(pg + (s0 + s) * 32);
-                    qu[s] = ld_stream_v2(pu + (s0 + s) * 32);
-                    fg[s] = ld_stream_u8(fgp + (s0 + s) * 4);
-                    fu[s] = ld_stream_u8(fup + (s0 + s) * 4);
+                if (t0 + s < nsup) {
+                    qg[s] = ld_stream_v4(pg + (t0 + s) * 64);
+                    qu[s] = ld_stream_v4(pu + (t0 + s) * 64);
+                    fg[s] = ld_stream_v2(fgp + (t0 + s) * 8);
+                    fu[s] = ld_stream_v2(fup + (t0 + s) * 8);
                 }
             }
 #pragma unroll
             for (int s = 0; s < kStagesFp4; ++s) {
-                const int seg = s0 + s;
-                if (seg < nseg) {
-                    uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
+                const int t = t0 + s;
+                if (t < nsup) {
+                    uint4 bq[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                                   make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
                     if (has_b) {
-                        const uint4* bp = reinterpret_cast<const uint4*>(xb + seg * 64);
-                        b0 = bp[0];
-                        b1 = bp[1];
-                    }
-                    const uint32_t sg2 = e4m3_splat_f16x2(fg[s]), su2 = e4m3_splat_f16x2(fu[s]);
-                    uint32_t ga[8], ua[8];
-                    e2m1x8_to_f16x2x4(qg[s].x, ga[0], ga[1], ga[2], ga[3]);
-                    e2m1x8_to_f16x2x4(qg[s].y, ga[4], ga[5], ga[6], ga[7]);
-                    e2m1x8_to_f16x2x4(qu[s].x, ua[0], ua[1], ua[2], ua[3]);
-                    e2m1x8_to_f16x2x4(qu[s].y, ua[4], ua[5], ua[6], ua[7]);
+                        const uint4* bp = reinterpret_cast<const uint4*>(xb4 + t * 128);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        ga[j] = hmul2(ga[j], sg2);
-                        ua[j] = hmul2(ua[j], su2);
+                        for (int j = 0; j < 4; ++j) bq[j] = bp[j];
                     }
-                    mma_f16(acc, ga[0], ua[0], ga[1], ua[1], b0.x, b0.y);
-                    mma_f16(acc, ga[2], ua[2], ga[3], ua[3], b0.z, b0.w);
-                    mma_f16(acc, ga[4], ua[4], ga[5], ua[5], b1.x, b1.y);
-                    mma_f16(acc, ga[6], ua[6], ga[7], ua[7], b1.z, b1.w);
+                    const uint32_t sgw = ((c >> 1) ? fg[s].y : fg[s].x) >> sf_shift;
+                    const uint32_t suw = ((c >> 1) ? fu[s].y : fu[s].x) >> sf_shift;
+                    const uint32_t wgq[4] = {qg[s].x, qg[s].y, qg[s].z, qg[s].w};
+                    const uint32_t wuq[4] = {qu[s].x, qu[s].y, qu[s].z, qu[s].w};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {          // elements 16h .. 16h+15 of the lane's 32
+                        const uint32_t sg2 = e4m3_splat_f16x2((sgw >> (8 * h)) & 0xFFu);
+                        const uint32_t su2 = e4m3_splat_f16x2((suw >> (8 * h)) & 0xFFu);
+                        uint32_t ga[8], ua[8];
+                        e2m1x8_to_f16x2x4(wgq[2 * h], ga[0], ga[1], ga[2], ga[3]);
+                        e2m1x8_to_f16x2x4(wgq[2 * h + 1], ga[4], ga[5], ga[6], ga[7]);
+                        e2m1x8_to_f16x2x4(wuq[2 * h], ua[0], ua[1], ua[2], ua[3]);
+                        e2m1x8_to_f16x2x4(wuq[2 * h + 1], ua[4], ua[5], ua[6], ua[7]);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            ga[j] = hmul2(ga[j], sg2);
+                            ua[j] = hmul2(ua[j], su2);
+                        }
+                        const uint4 b0 = bq[2 * h], b1 = bq[2 * h + 1];
+                        mma_f16(acc, ga[0], ua[0], ga[1], ua[1], b0.x, b0.y);
+                        mma_f16(acc, ga[2], ua[2], ga[3], ua[3], b0.z, b0.w);
+                        mma_f16(acc, ga[4], ua[4], ga[5], ua[5], b1.x, b1.y);
+                        mma_f16(acc, ga[6], ua[6], ga[7], ua[7], b1.z, b1.w);
+                    }
                 }
             }
         }
@@ -378,19 +399,25 @@ __device__ void down_item(const DownArgs& a, const GroupList& gl, int jt, float*
             const size_t r0 = static_cast<size_t>(e) * H + j0 + g;
             const uint8_t* pa0 = a.wd + r0 * (I / 2) + c * 8;
             const uint8_t* pa1 = pa0 + static_cast<size_t>(8) * (I / 2);
-            const uint8_t* fa0 = a.sfd + r0 * (I / 16) + c;
+            // the row's scale bytes of two segments come in one 8-byte load shared by its 4 lanes
+            const uint8_t* fa0 = a.sfd + r0 * (I / 16);
             const uint8_t* fa1 = fa0 + static_cast<size_t>(8) * (I / 16);
             constexpr int kS = 2 * kStages;
             for (int s0 = 0; s0 < nseg; s0 += kS) {
                 uint2 qa[kS], qb[kS];
-                uint32_t fa[kS], fb[kS];
+                uint2 fa2[kS / 2], fb2[kS / 2];
 #pragma unroll
                 for (int s = 0; s < kS; ++s) {
                     if (s0 + s < nseg) {
                         qa[s] = ld_stream_v2(pa0 + (s0 + s) * 32);
                         qb[s] = ld_stream_v2(pa1 + (s0 + s) * 32);
-                        fa[s] = ld_stream_u8(fa0 + (s0 + s) * 4);
-                        fb[s] = ld_stream_u8(fa1 + (s0 + s) * 4);
+                    }
+                }
+#pragma unroll
+                for (int s = 0; s < kS; s += 2) {
+                    if (s0 + s < nseg) {
+                        fa2[s / 2] = ld_stream_v2(fa0 + (s0 + s) * 4);
+                        fb2[s / 2] = ld_stream_v2(fa1 + (s0 + s) * 4);
                     }
                 }
                 if (kWaitDeps && !waited) {
@@ -407,7 +434,10 @@ __device__ void down_item(const DownArgs& a, const GroupList& gl, int jt, float*
                             b0 = bp[0];
                             b1 = bp[1];
                         }
-                        const uint32_t sa = e4m3_splat_f16x2(fa[s]), sb = e4m3_splat_f16x2(fb[s]);
+                        const uint32_t wa_ = (s & 1) ? fa2[s / 2].y : fa2[s / 2].x;
+                        const uint32_t wb_ = (s & 1) ? fb2[s / 2].y : fb2[s / 2].x;
+                        const uint32_t sa = e4m3_splat_f16x2((wa_ >> (8 * c)) & 0xFFu);
+                        const uint32_t sb = e4m3_splat_f16x2((wb_ >> (8 * c)) & 0xFFu);
                         uint32_t xa[8], xb[8];
                         e2m1x8_to_f16x2x4(qa[s].x, xa[0], xa[1], xa[2], xa[3]);
                         e2m1x8_to_f16x2x4(qa[s].y, xa[4], xa[5], xa[6], xa[7]);

@@ -8,7 +8,8 @@
 //                 programmatic dependent that starts its weight stream while gate_up drains.
 //   2 <= T <= 8 : one fused cooperative launch (fused.cu): in-kernel expert grouping, gate/up +
 //                 SwiGLU, grid barrier, down + slot-order combine (after a 4-byte barrier memset).
-//   T > 8       : even row groups of <= 8 tokens ("forward.rs", `moe_row_groups`), each as above.
+//   T > 8, FP8  : grouped GEMMs over expert-sorted rows (prefill.cu).
+//   T > 8, NVFP4: even row groups of <= 8 tokens ("forward.rs", `moe_row_groups`), each as above.
 // The stage entry points (moe_plan, moe_*_gate_up, moe_*_down_combine) run the same work items
 // as separate kernels and give the same bits.
 #include <cmath>
@@ -38,6 +39,14 @@ bool shape_ok(int T, int H, int I, int E, int topk) {
 }
 
 int rows_per_sweep(int T) { return T < kMaxRowsPerSweep ? T : kMaxRowsPerSweep; }
+
+// The grouped-GEMM (prefill) tier: FP8 weights, more than one 8-token sweep, and shapes its
+// tiles cover (per-K-block scale tables of <= 64 entries).
+bool uses_prefill(int T, int H, int I, int E, int fmt) {
+    return fmt == 0 && T > kMaxRowsPerSweep && H <= 8192 && I <= 8192 && E <= kMaxPlanExperts &&
+           static_cast<long long>(T) * kMaxTopk < (1LL << 30);
+}
+
 
 // Largest number of columns a group can have for a sub-batch of `rows` tokens.
 int group_cap(int rows, int topk) {
@@ -214,6 +223,15 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
             size_t ws_bytes, int32_t* err, cudaStream_t s) {
     int rc = check_sizes(T, H, I, E, topk);
     if (rc) return rc;
+    if (FMT == 0 && uses_prefill(T, H, I, E, 0)) {
+        if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
+        const PrefillLayout L = prefill_layout(T, H, I, E, topk);
+        if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+        return cuda_status(launch_prefill_fp8(
+            reinterpret_cast<const __nv_bfloat16*>(x), T, H, I, E, topk, ids, wts, pg.w, pg.s, pu.w,
+            pu.s, pd.w, pd.s, limit, reinterpret_cast<__nv_bfloat16*>(out),
+            static_cast<uint8_t*>(ws), L, err, s));
+    }
     const int rows_max = rows_per_sweep(T);
     Ws w;
     if ((rc = check_ws(ws, ws_bytes, rows_max, I, E, topk, w))) return rc;
@@ -260,6 +278,8 @@ extern "C" {
 size_t moe_workspace_bytes(int T, int H, int I, int E, int topk, int fmt) {
     if (fmt != MOE_FMT_FP8_E4M3_B128 && fmt != MOE_FMT_NVFP4) return 0;
     if (check_sizes(T, H, I, E, topk) != MOE_OK) return 0;
+    if (uses_prefill(T, H, I, E, fmt == MOE_FMT_FP8_E4M3_B128 ? 0 : 1))
+        return prefill_layout(T, H, I, E, topk).total;
     return ws_layout(rows_per_sweep(T), I, E, topk).total;
 }
 

@@ -51,6 +51,19 @@ template <int FMT> cudaError_t launch_fused_forward(const GateUpArgs& ga, const 
                                                     cudaStream_t stream);
 size_t fused_smem_bytes(int H, int rows, int topk, int cap);
 
+// Wide tier (prefill.cu): workspace layout and the launch sequence of the grouped-GEMM path.
+struct PrefillLayout {
+    size_t counts, offsets, sorted_pair, pair_to_sorted, tiles, tile_e, tile_r0;
+    size_t x16, xinv, amax, a16, ainv, f32, total;
+};
+PrefillLayout prefill_layout(int T, int H, int I, int E, int topk);
+cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
+                               const int32_t* ids, const float* wts, const uint8_t* wg,
+                               const float* sg, const uint8_t* wu, const float* su,
+                               const uint8_t* wd, const float* sd, float limit,
+                               __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L,
+                               int32_t* err, cudaStream_t stream);
+
 // Route histogram / stable counting sort, optionally emitting expert groups (route_plan.cu).
 cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,
                               int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,

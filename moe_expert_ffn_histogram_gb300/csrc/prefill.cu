@@ -1,0 +1,518 @@
+// Wide (prefill) tier: the routed pairs of a whole batch, sorted by expert, go through two
+// grouped GEMMs instead of per-token GEMV sweeps, so each expert's weights are read once per
+// 128-row tile of its routed rows rather than once per 8 tokens.
+//
+// "spark_model layers/glm5next_mlp/forward.rs": `forward_moe` sends rows > 8 (and above a
+// measured width floor) to the grouped tensor-core GEMM over expert-sorted rows, one launch per
+// projection, with `moe_sort_by_expert` before it and the `_indexed` combine after it (same slot
+// order and rounding as the narrow tiers). Here:
+//
+//   route_plan (existing)    counts / offsets / sorted_pair / pair_to_sorted
+//   prefill_tiles            the m-tile list: (expert, first sorted row) per 128-row tile
+//   prefill_x_prep           x (bf16) -> x16 (f16, one power-of-two range scale per token)
+//   prefill_gateup_gemm      per tile of 128 sorted rows x 64 features: gate and up from the
+//                            same weight tile walk, clamped SwiGLU in the epilogue -> a (fp32) and
+//                            a per-row running max |a|
+//   prefill_act_prep         a (fp32) -> a16 (f16, one power-of-two range scale per sorted row)
+//   prefill_down_gemm        per tile of 128 sorted rows x 128 output columns: y (fp32)
+//   prefill_combine          out[t] = sum over slots k in order of w[t,k] * y[pair_to_sorted], bf16
+//
+// Weights are dequantised while building MMA fragments: E4M3 -> f16 exactly, times the block
+// scale pre-multiplied by a power of two chosen per (expert, 128-row weight block) so the product
+// stays in f16's normal range (one f16 rounding per weight); the power of two is undone in the
+// fp32 epilogue. Products accumulate in fp32.
+#include "gemv_items.cuh"
+
+namespace moe {
+
+namespace prefill {
+
+constexpr int kBM = 128;               // sorted rows per tile
+constexpr int kBN = 128;               // weight rows per tile (gate/up: 64 gate + the same 64 up)
+constexpr int kBK = 64;                // K per pipeline stage
+constexpr int kThreads = 256;          // 8 warps: 2 (rows) x 4 (columns), warp tile 64 x 32
+constexpr int kStages = 3;
+constexpr int kARow = kBK * 2 + 32;    // A smem row pitch in bytes (f16 + 32 B pad: no conflicts)
+constexpr int kBRow = kBK + 16;        // B smem row pitch in bytes (fp8 + 16 B pad: no conflicts)
+constexpr int kAStage = kBM * kARow;
+constexpr int kBStage = kBN * kBRow;
+constexpr int kSmem = kStages * (kAStage + kBStage);
+
+}  // namespace prefill
+
+// ---- tile list -----------------------------------------------------------------------------------
+
+// One block: m-tile list from the per-expert counts (ascending expert, 128 sorted rows per tile).
+// tiles[0] = number of m-tiles; tile_e[i], tile_r0[i] = expert and first sorted row of tile i.
+__global__ void __launch_bounds__(1024) prefill_tiles_kernel(const int32_t* __restrict__ counts,
+                                                             const int32_t* __restrict__ offsets,
+                                                             int E, int32_t* __restrict__ tiles,
+                                                             int32_t* __restrict__ tile_e,
+                                                             int32_t* __restrict__ tile_r0) {
+    __shared__ int warp_sum[32];
+    __shared__ int base_s;
+    if (threadIdx.x == 0) base_s = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        const int n = e < E ? (counts[e] + prefill::kBM - 1) / prefill::kBM : 0;
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int v = lane < (blockDim.x >> 5) ? warp_sum[lane] : 0;
+            int wi = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += u;
+            }
+            warp_sum[lane] = wi - v;
+        }
+        __syncthreads();
+        const int start = base_s + warp_sum[warp] + incl - n;
+        for (int i = 0; i < n; ++i) {
+            tile_e[start + i] = e;
+            tile_r0[start + i] = offsets[e] + i * prefill::kBM;
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) base_s = start + n;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) tiles[0] = base_s;
+}
+
+// ---- x prep ---------------------------------------------------------------------------------------
+
+// One block per token: x16[t] = f16(x[t] * s_t), xinv[t] = 1 / s_t, s_t a power of two.
+__global__ void __launch_bounds__(256) prefill_x_prep_kernel(const __nv_bfloat16* __restrict__ x,
+                                                             int H, __half* __restrict__ x16,
+                                                             float* __restrict__ xinv) {
+    __shared__ float red[8];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    const int nv = H / 8;
+    float m = 0.0f;
+    for (int v = tid; v < nv; v += 256) {
+        const uint4 q = __ldg(xr + v);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+            m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        }
+    }
+    m = warp_max(m);
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    float mm = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mm = fmaxf(mm, red[w]);
+    float inv;
+    const float s = pow2_range_scale(mm, inv);
+    if (tid == 0) xinv[t] = inv;
+    uint4* dst = reinterpret_cast<uint4*>(x16 + static_cast<size_t>(t) * H);
+    for (int v = tid; v < nv; v += 256) {
+        const uint4 q = __ldg(xr + v);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h2 = __floats2half2_rn(__uint_as_float(w[i] << 16) * s,
+                                                 __uint_as_float(w[i] & 0xFFFF0000u) * s);
+            o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// ---- activation prep -------------------------------------------------------------------------------
+
+// One block per sorted row: a16[r] = f16(a[r] * s_r), ainv[r] = 1 / s_r, from the row's max |a|
+// (kept as the float's bit pattern by the gate/up GEMM's integer atomicMax).
+__global__ void __launch_bounds__(256) prefill_act_prep_kernel(const float* __restrict__ a32,
+                                                               const uint32_t* __restrict__ amax,
+                                                               const int32_t* __restrict__ nrows,
+                                                               int I, __half* __restrict__ a16,
+                                                               float* __restrict__ ainv) {
+    const int r = blockIdx.x;
+    if (r >= *nrows) return;
+    float inv;
+    const float s = pow2_range_scale(__uint_as_float(amax[r]), inv);
+    if (threadIdx.x == 0) ainv[r] = inv;
+    const float4* src = reinterpret_cast<const float4*>(a32 + static_cast<size_t>(r) * I);
+    uint2* dst = reinterpret_cast<uint2*>(a16 + static_cast<size_t>(r) * I);
+    for (int v = threadIdx.x; v < I / 4; v += 256) {
+        const float4 q = src[v];
+        const __half2 lo = __floats2half2_rn(q.x * s, q.y * s), hi = __floats2half2_rn(q.z * s, q.w * s);
+        dst[v] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
+}
+
+// ---- combine ----------------------------------------------------------------------------------------
+
+// out[t][j] = bf16( sum_{k in slot order} w[t,k] * y[pair_to_sorted[t*topk+k]][j] ), a separate
+// rounded multiply and add per term (ep_step_fp8_gate.rs, `combine_down_rows_host`; the indexed
+// twin of forward.rs's `glm5next_moe_combine_indexed`). One block per token.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ y,
+                                                              const int32_t* __restrict__ pair_to_sorted,
+                                                              const float* __restrict__ wts,
+                                                              int topk, int H,
+                                                              __nv_bfloat16* __restrict__ out) {
+    const int t = blockIdx.x;
+    int rows[kMaxTopk];
+    float w[kMaxTopk];
+#pragma unroll
+    for (int k = 0; k < kMaxTopk; ++k) {
+        rows[k] = k < topk ? pair_to_sorted[t * topk + k] : -1;
+        w[k] = k < topk ? wts[t * topk + k] : 0.0f;
+    }
+    for (int j = threadIdx.x * 4; j < H; j += 256 * 4) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kMaxTopk; ++k) {
+            if (rows[k] < 0) continue;
+            const float4 v = *reinterpret_cast<const float4*>(y + static_cast<size_t>(rows[k]) * H + j);
+            s[0] = __fadd_rn(s[0], __fmul_rn(w[k], v.x));
+            s[1] = __fadd_rn(s[1], __fmul_rn(w[k], v.y));
+            s[2] = __fadd_rn(s[2], __fmul_rn(w[k], v.z));
+            s[3] = __fadd_rn(s[3], __fmul_rn(w[k], v.w));
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(s[0], s[1]), hi = __floats2bfloat162_rn(s[2], s[3]);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&lo);
+        o.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + static_cast<size_t>(t) * H + j) = o;
+    }
+}
+
+// ---- grouped GEMMs (mma.sync m16n8k16 f16 -> f32) ------------------------------------------------
+
+struct PrefillGemmArgs {
+    // tile schedule
+    const int32_t* tiles;        // [1] number of m-tiles
+    const int32_t* tile_e;       // [m-tiles]
+    const int32_t* tile_r0;      // [m-tiles]
+    const int32_t* offsets;      // [E+1]
+    const int32_t* sorted_pair;  // [P]
+    int topk, K, n_tiles;
+    // A operand: rows of a16 (KIND 1) or rows of x16 gathered through sorted_pair (KIND 0)
+    const __half* a;
+    const float* a_inv;          // per token (KIND 0) or per sorted row (KIND 1)
+    // B operand: E4M3 weight rows and fp32 block scales; KIND 0 uses both gate (w0) and up (w1)
+    const uint8_t* w0;
+    const float* s0;
+    const uint8_t* w1;
+    const float* s1;
+    int wrows;                   // rows of one expert's weight matrix (I for gate/up, H for down)
+    float limit;
+    // outputs
+    float* out;                  // KIND 0: a32 [P][I]; KIND 1: y [P][H]
+    uint32_t* amax;              // KIND 0: per sorted row max |a| (float bits), zeroed before
+    int out_ld;                  // I (KIND 0) or H (KIND 1)
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(prefill::kThreads, 2) prefill_gemm_kernel(const PrefillGemmArgs p) {
+    using namespace prefill;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t* sa = smem;                               // [kStages][kBM][kARow]
+    uint8_t* sb = smem + kStages * kAStage;           // [kStages][kBN][kBRow]
+    __shared__ const __half* a_row[kBM];              // A row sources of this tile
+    __shared__ float a_scale[kBM];                    // their inverse range scales
+    __shared__ uint32_t w_scale[2][64];               // per 128-wide K block: f16x2 splat of the
+                                                      // prescaled block scale (gate/down, up)
+    __shared__ float w_inv[2];                        // the inverse of the power-of-two prescale
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int wm = warp >> 2, wn = warp & 3;
+    const int K = p.K, KT = K / kBK, KB = K / 128;
+    const int total = p.tiles[0] * p.n_tiles;
+
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+        const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
+        const int rows = min(kBM, p.offsets[e + 1] - r0);
+
+        // ---- per-tile tables: A row sources and scales, weight block scales ----
+        __syncthreads();                              // previous tile's readers are done
+        if (tid < kBM) {
+            const int r = r0 + min(tid, rows - 1);    // padded rows repeat the last valid row
+            if (KIND == 0) {
+                const int t = p.sorted_pair[r] / p.topk;
+                a_row[tid] = p.a + static_cast<size_t>(t) * K;
+                a_scale[tid] = p.a_inv[t];
+            } else {
+                a_row[tid] = p.a + static_cast<size_t>(r) * K;
+                a_scale[tid] = p.a_inv[r];
+            }
+        }
+        if (warp < 2) {                               // warp 0: gate/down scales, warp 1: up
+            const int nb = KIND == 0 ? (nt * 64) / 128 : nt;
+            const float* srow = (warp == 0 ? p.s0 : p.s1) + (static_cast<size_t>(e) * (p.wrows / 128) + nb) * KB;
+            if (KIND == 1 && warp == 1) srow = p.s0 + (static_cast<size_t>(e) * (p.wrows / 128) + nb) * KB;
+            float m = 0.0f;
+            for (int kb = lane; kb < KB; kb += 32) m = fmaxf(m, fabsf(srow[kb]));
+            m = warp_max(m) * 448.0f;
+            float inv;
+            const float pre = pow2_range_scale(m, inv);
+            for (int kb = lane; kb < KB; kb += 32) {
+                const __half h = __float2half_rn(srow[kb] * pre);
+                const uint16_t hb = *reinterpret_cast<const uint16_t*>(&h);
+                w_scale[warp][kb] = static_cast<uint32_t>(hb) * 0x10001u;
+            }
+            if (lane == 0) w_inv[warp] = inv;
+        }
+        __syncthreads();
+
+        // ---- loader: stage s <- K slice kt ----
+        auto load = [&](int kt, int s) {
+            uint8_t* dA = sa + s * kAStage;
+            uint8_t* dB = sb + s * kBStage;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {             // A: 128 rows x 8 chunks of 16 B
+                const int ch = tid + i * kThreads, r = ch >> 3, q = ch & 7;
+                cp_async16(dA + r * kARow + q * 16, a_row[r] + kt * kBK + q * 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {             // B: 128 weight rows x 4 chunks of 16 B
+                const int ch = tid + i * kThreads, n = ch >> 2, q = ch & 3;
+                const uint8_t* src;
+                if (KIND == 0) {
+                    // tile row n -> warp column group j, fragment f, row gg: fragments 0,1 are gate
+                    // rows and 2,3 the matching up rows of the same 16 features
+                    const int j = n >> 5, f = (n & 31) >> 3, gg = n & 7;
+                    const int feat = nt * 64 + 16 * j + 8 * (f & 1) + gg;
+                    src = (f < 2 ? p.w0 : p.w1) + (static_cast<size_t>(e) * p.wrows + feat) * K;
+                } else {
+                    src = p.w0 + (static_cast<size_t>(e) * p.wrows + nt * kBN + n) * K;
+                }
+                cp_async16(dB + n * kBRow + q * 16, src + kt * kBK + q * 16);
+            }
+        };
+
+        float acc[4][4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int f = 0; f < 4; ++f)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[i][f][r] = 0.0f;
+
+        load(0, 0);
+        cp_async_commit();
+        if (KT > 1) load(1, 1);
+        cp_async_commit();
+        for (int kt = 0; kt < KT; ++kt) {
+            cp_async_wait<1>();
+            __syncthreads();
+            if (kt + 2 < KT) load(kt + 2, (kt + 2) % kStages);
+            cp_async_commit();
+            const uint8_t* A = sa + (kt % kStages) * kAStage;
+            const uint8_t* B = sb + (kt % kStages) * kBStage;
+            const uint32_t sc0 = w_scale[0][(kt * kBK) / 128];
+            const uint32_t sc1 = KIND == 0 ? w_scale[1][(kt * kBK) / 128] : sc0;
+#pragma unroll
+            for (int q = 0; q < kBK / 16; ++q) {
+                uint32_t af[4][4], bf[4][2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = wm * 64 + 16 * i + g;
+                    const uint2 lo = lds64(A + row * kARow + (q * 16 + 4 * c) * 2);
+                    const uint2 hi = lds64(A + (row + 8) * kARow + (q * 16 + 4 * c) * 2);
+                    af[i][0] = lo.x;
+                    af[i][1] = hi.x;
+                    af[i][2] = lo.y;
+                    af[i][3] = hi.y;
+                }
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    const int n = wn * 32 + 8 * f + g;
+                    const uint32_t w4 = *reinterpret_cast<const uint32_t*>(B + n * kBRow + q * 16 + 4 * c);
+                    uint32_t lo, hi;
+                    e4m3x4_to_f16x2x2(w4, lo, hi);
+                    const uint32_t sc = (KIND == 0 && f >= 2) ? sc1 : sc0;
+                    bf[f][0] = hmul2(lo, sc);
+                    bf[f][1] = hmul2(hi, sc);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        mma_f16(acc[i][f], af[i][0], af[i][1], af[i][2], af[i][3], bf[f][0], bf[f][1]);
+            }
+        }
+        cp_async_wait<0>();
+
+        // ---- epilogue ----
+        if (KIND == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int hrow = 0; hrow < 2; ++hrow) {
+                    const int row = wm * 64 + 16 * i + g + 8 * hrow;
+                    const float xs = a_scale[row];
+                    float m = 0.0f;
+                    float hv[2][2];
+#pragma unroll
+                    for (int f = 0; f < 2; ++f)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const float gv = acc[i][f][2 * hrow + j] * xs * w_inv[0];
+                            const float uv = acc[i][f + 2][2 * hrow + j] * xs * w_inv[1];
+                            hv[f][j] = clamped_swiglu(gv, uv, p.limit);
+                            m = fmaxf(m, fabsf(hv[f][j]));
+                        }
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    if (row < rows) {
+                        float* dst = p.out + static_cast<size_t>(r0 + row) * p.out_ld + nt * 64 + 16 * wn;
+#pragma unroll
+                        for (int f = 0; f < 2; ++f)
+                            *reinterpret_cast<float2*>(dst + 8 * f + 2 * c) = make_float2(hv[f][0], hv[f][1]);
+                        if (c == 0) atomicMax(p.amax + r0 + row, __float_as_uint(m));
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int hrow = 0; hrow < 2; ++hrow) {
+                    const int row = wm * 64 + 16 * i + g + 8 * hrow;
+                    if (row >= rows) continue;
+                    const float sc = a_scale[row] * w_inv[0];
+                    float* dst = p.out + static_cast<size_t>(r0 + row) * p.out_ld + nt * kBN + wn * 32;
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        *reinterpret_cast<float2*>(dst + 8 * f + 2 * c) =
+                            make_float2(acc[i][f][2 * hrow] * sc, acc[i][f][2 * hrow + 1] * sc);
+                }
+            }
+        }
+    }
+}
+
+// ---- workspace and launch sequence ------------------------------------------------------------------
+
+PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
+    const size_t P = static_cast<size_t>(T) * topk;
+    const size_t mtiles = P / prefill::kBM + static_cast<size_t>(E) + 1;
+    PrefillLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    L.counts = take(static_cast<size_t>(E) * 4);
+    L.offsets = take((static_cast<size_t>(E) + 1) * 4);
+    L.sorted_pair = take(P * 4);
+    L.pair_to_sorted = take(P * 4);
+    L.tiles = take(16);
+    L.tile_e = take(mtiles * 4);
+    L.tile_r0 = take(mtiles * 4);
+    L.x16 = take(static_cast<size_t>(T) * H * 2);
+    L.xinv = take(static_cast<size_t>(T) * 4);
+    L.amax = take(P * 4);
+    L.a16 = take(P * static_cast<size_t>(I) * 2);
+    L.ainv = take(P * 4);
+    L.f32 = take(P * static_cast<size_t>(H > I ? H : I) * 4);   // a (fp32), later y
+    L.total = o;
+    return L;
+}
+
+namespace {
+
+int gemm_grid() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return 2 * sms;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
+                               const int32_t* ids, const float* wts, const uint8_t* wg,
+                               const float* sg, const uint8_t* wu, const float* su,
+                               const uint8_t* wd, const float* sd, float limit,
+                               __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L,
+                               int32_t* err, cudaStream_t stream) {
+    const int P = T * topk;
+    auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+    cudaError_t st;
+    if ((st = launch_route_plan(ids, P, E, 1, I32(L.counts), I32(L.offsets), I32(L.sorted_pair),
+                                I32(L.pair_to_sorted), nullptr, nullptr, nullptr, nullptr, err,
+                                stream)) != cudaSuccess)
+        return st;
+    prefill_tiles_kernel<<<1, 1024, 0, stream>>>(I32(L.counts), I32(L.offsets), E, I32(L.tiles),
+                                                 I32(L.tile_e), I32(L.tile_r0));
+    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
+    float* xinv = reinterpret_cast<float*>(ws + L.xinv);
+    prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv);
+    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
+    if ((st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess) return st;
+
+    const int grid = gemm_grid();
+    if (grid <= 0) return cudaErrorInvalidDevice;
+    if ((st = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   prefill::kSmem)) != cudaSuccess)
+        return st;
+    if ((st = cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   prefill::kSmem)) != cudaSuccess)
+        return st;
+    float* f32 = reinterpret_cast<float*>(ws + L.f32);
+    PrefillGemmArgs gu{};
+    gu.tiles = I32(L.tiles);
+    gu.tile_e = I32(L.tile_e);
+    gu.tile_r0 = I32(L.tile_r0);
+    gu.offsets = I32(L.offsets);
+    gu.sorted_pair = I32(L.sorted_pair);
+    gu.topk = topk;
+    gu.K = H;
+    gu.n_tiles = I / 64;
+    gu.a = x16;
+    gu.a_inv = xinv;
+    gu.w0 = wg;
+    gu.s0 = sg;
+    gu.w1 = wu;
+    gu.s1 = su;
+    gu.wrows = I;
+    gu.limit = limit;
+    gu.out = f32;
+    gu.amax = amax;
+    gu.out_ld = I;
+    prefill_gemm_kernel<0><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(gu);
+    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+
+    __half* a16 = reinterpret_cast<__half*>(ws + L.a16);
+    float* ainv = reinterpret_cast<float*>(ws + L.ainv);
+    prefill_act_prep_kernel<<<P, 256, 0, stream>>>(f32, amax, I32(L.offsets) + E, I, a16, ainv);
+    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+
+    PrefillGemmArgs dn = gu;
+    dn.K = I;
+    dn.n_tiles = H / prefill::kBN;
+    dn.a = a16;
+    dn.a_inv = ainv;
+    dn.w0 = wd;
+    dn.s0 = sd;
+    dn.w1 = wd;
+    dn.s1 = sd;
+    dn.wrows = H;
+    dn.out = f32;
+    dn.amax = nullptr;
+    dn.out_ld = H;
+    prefill_gemm_kernel<1><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(dn);
+    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+
+    prefill_combine_kernel<<<T, 256, 0, stream>>>(f32, I32(L.pair_to_sorted), wts, topk, H, out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -245,3 +245,41 @@ def test_nvfp4_decode_full_size():
     for rs in range(2):
         wl = inputs.make_workload("nvfp4_decode", device=DEV, bank=bank, route_set=rs)
         check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"nvfp4_decode set {rs}")
+
+
+# ---- the grouped-GEMM (prefill) tier: FP8, T > 8 ----------------------------------------------------
+
+@pytest.mark.parametrize("T,H,I,E,routes", [(9, 256, 128, 16, "uniform"), (64, 384, 256, 40, "zipf"),
+                                            (300, 256, 256, 8, "uniform"), (130, 512, 384, 24, "zipf")])
+def test_prefill_parity(T, H, I, E, routes):
+    wl = inputs.make_custom("fp8", T, H, I, E, seed=700 + T, device=DEV, routes=routes)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"prefill T={T} E={E}")
+
+
+def test_prefill_skewed_and_bad_ids():
+    T, E = 200, 12
+    wl = inputs.make_custom("fp8", T, 256, 256, E, seed=801, device=DEV)
+    ids = wl.ids.clone()
+    ids[:150, :4] = torch.tensor([0, 1, 2, 3], dtype=torch.int32, device=DEV)   # experts 0..3 get 150+ rows
+    ids[5, 6] = -1
+    ids[7, 2] = E + 3
+    wl.ids = ids
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(wl, err=err)
+    assert int(err.item()) & capi.ERRBIT_BAD_ID
+    check_close(bf16_to_f64(out), oracle_for(wl)["out"], "prefill skew")
+
+
+def test_prefill_clamp_stress_and_no_limit():
+    wl = inputs.make_custom("fp8", 40, 256, 256, 10, seed=802, device=DEV, x_scale=40.0)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], "prefill clamp stress")
+    wl2 = inputs.make_custom("fp8", 24, 256, 128, 10, seed=803, device=DEV, x_scale=20.0,
+                             limit=float("inf"))
+    check_close(bf16_to_f64(run(wl2)), oracle_for(wl2)["out"], "prefill no limit")
+
+
+def test_prefill_bitwise_repeatable():
+    wl = inputs.make_custom("fp8", 100, 256, 256, 16, seed=804, device=DEV, routes="zipf")
+    a = run(wl).clone()
+    for _ in range(2):
+        assert torch.equal(run(wl).view(torch.int16), a.view(torch.int16))

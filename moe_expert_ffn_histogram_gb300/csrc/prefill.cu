@@ -21,24 +21,16 @@
 // scale pre-multiplied by a power of two chosen per (expert, 128-row weight block) so the product
 // stays in f16's normal range (one f16 rounding per weight); the power of two is undone in the
 // fp32 epilogue. Products accumulate in fp32.
-#include "gemv_items.cuh"
+#include "prefill.cuh"
+
+// Which grouped-GEMM core the prefill tier launches: 1 = tcgen05/TMEM (prefill_tc.cu),
+// 0 = mma.sync (below).
+#ifndef MOE_PREFILL_TC
+#define MOE_PREFILL_TC 0
+#endif
 
 namespace moe {
 
-namespace prefill {
-
-constexpr int kBM = 128;               // sorted rows per tile
-constexpr int kBN = 128;               // weight rows per tile (gate/up: 64 gate + the same 64 up)
-constexpr int kBK = 64;                // K per pipeline stage
-constexpr int kThreads = 256;          // 8 warps: 2 (rows) x 4 (columns), warp tile 64 x 32
-constexpr int kStages = 3;
-constexpr int kARow = kBK * 2 + 32;    // A smem row pitch in bytes (f16 + 32 B pad: no conflicts)
-constexpr int kBRow = kBK + 16;        // B smem row pitch in bytes (fp8 + 16 B pad: no conflicts)
-constexpr int kAStage = kBM * kARow;
-constexpr int kBStage = kBN * kBRow;
-constexpr int kSmem = kStages * (kAStage + kBStage);
-
-}  // namespace prefill
 
 // ---- tile list -----------------------------------------------------------------------------------
 
@@ -194,29 +186,6 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
 
 // ---- grouped GEMMs (mma.sync m16n8k16 f16 -> f32) ------------------------------------------------
 
-struct PrefillGemmArgs {
-    // tile schedule
-    const int32_t* tiles;        // [1] number of m-tiles
-    const int32_t* tile_e;       // [m-tiles]
-    const int32_t* tile_r0;      // [m-tiles]
-    const int32_t* offsets;      // [E+1]
-    const int32_t* sorted_pair;  // [P]
-    int topk, K, n_tiles;
-    // A operand: rows of a16 (KIND 1) or rows of x16 gathered through sorted_pair (KIND 0)
-    const __half* a;
-    const float* a_inv;          // per token (KIND 0) or per sorted row (KIND 1)
-    // B operand: E4M3 weight rows and fp32 block scales; KIND 0 uses both gate (w0) and up (w1)
-    const uint8_t* w0;
-    const float* s0;
-    const uint8_t* w1;
-    const float* s1;
-    int wrows;                   // rows of one expert's weight matrix (I for gate/up, H for down)
-    float limit;
-    // outputs
-    float* out;                  // KIND 0: a32 [P][I]; KIND 1: y [P][H]
-    uint32_t* amax;              // KIND 0: per sorted row max |a| (float bits), zeroed before
-    int out_ld;                  // I (KIND 0) or H (KIND 1)
-};
 
 template <int KIND>
 __global__ void __launch_bounds__(prefill::kThreads, 2) prefill_gemm_kernel(const PrefillGemmArgs p) {
@@ -487,8 +456,13 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     gu.out = f32;
     gu.amax = amax;
     gu.out_ld = I;
-    prefill_gemm_kernel<0><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(gu);
-    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    gu.err = err;
+    if (MOE_PREFILL_TC) {
+        if ((st = launch_prefill_gemm_tc(0, gu, stream)) != cudaSuccess) return st;
+    } else {
+        prefill_gemm_kernel<0><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(gu);
+        if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    }
 
     __half* a16 = reinterpret_cast<__half*>(ws + L.a16);
     float* ainv = reinterpret_cast<float*>(ws + L.ainv);
@@ -508,8 +482,12 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     dn.out = f32;
     dn.amax = nullptr;
     dn.out_ld = H;
-    prefill_gemm_kernel<1><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(dn);
-    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    if (MOE_PREFILL_TC) {
+        if ((st = launch_prefill_gemm_tc(1, dn, stream)) != cudaSuccess) return st;
+    } else {
+        prefill_gemm_kernel<1><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(dn);
+        if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    }
 
     prefill_combine_kernel<<<T, 256, 0, stream>>>(f32, I32(L.pair_to_sorted), wts, topk, H, out);
     return cudaGetLastError();

@@ -45,7 +45,10 @@ struct PrefillGemmArgs {
     int32_t* err;                // optional error word (bit 1: a bounded wait gave up)
 };
 
-// Launch one grouped GEMM (KIND 0: gate/up + SwiGLU, KIND 1: down) on the tcgen05 core.
+// Launch one grouped GEMM (KIND 0: gate/up + SwiGLU, KIND 1: down) on the simple tcgen05 core
+// (prefill_tc.cu) or the warp-specialised one (prefill_ws.cu; N_total = I or H, it picks its own
+// column tiling and sets n_tiles).
 cudaError_t launch_prefill_gemm_tc(int kind, const PrefillGemmArgs& p, cudaStream_t stream);
+cudaError_t launch_prefill_gemm_ws(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
 
 }  // namespace moe

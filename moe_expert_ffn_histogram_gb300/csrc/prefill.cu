@@ -23,10 +23,11 @@
 // fp32 epilogue. Products accumulate in fp32.
 #include "prefill.cuh"
 
-// Which grouped-GEMM core the prefill tier launches: 2 = warp-specialised tcgen05/TMEM
-// (prefill_ws.cu), 1 = simple tcgen05/TMEM (prefill_tc.cu), 0 = mma.sync (below).
+// Which grouped-GEMM core the prefill tier launches: 3 = TMA-fed warp-specialised tcgen05/TMEM
+// (prefill_tma.cu), 2 = cp.async-fed warp-specialised (prefill_ws.cu), 1 = simple tcgen05/TMEM
+// (prefill_tc.cu), 0 = mma.sync (below).
 #ifndef MOE_PREFILL_TC
-#define MOE_PREFILL_TC 2
+#define MOE_PREFILL_TC 3
 #endif
 
 namespace moe {
@@ -457,7 +458,11 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     gu.amax = amax;
     gu.out_ld = I;
     gu.err = err;
-    if (MOE_PREFILL_TC == 2) {
+    gu.a_rows = T;
+    gu.experts = E;
+    if (MOE_PREFILL_TC == 3) {
+        if ((st = launch_prefill_gemm_tma(0, gu, I, stream)) != cudaSuccess) return st;
+    } else if (MOE_PREFILL_TC == 2) {
         if ((st = launch_prefill_gemm_ws(0, gu, I, stream)) != cudaSuccess) return st;
     } else if (MOE_PREFILL_TC == 1) {
         if ((st = launch_prefill_gemm_tc(0, gu, stream)) != cudaSuccess) return st;
@@ -484,7 +489,10 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     dn.out = f32;
     dn.amax = nullptr;
     dn.out_ld = H;
-    if (MOE_PREFILL_TC == 2) {
+    dn.a_rows = P;
+    if (MOE_PREFILL_TC == 3) {
+        if ((st = launch_prefill_gemm_tma(1, dn, H, stream)) != cudaSuccess) return st;
+    } else if (MOE_PREFILL_TC == 2) {
         if ((st = launch_prefill_gemm_ws(1, dn, H, stream)) != cudaSuccess) return st;
     } else if (MOE_PREFILL_TC == 1) {
         if ((st = launch_prefill_gemm_tc(1, dn, stream)) != cudaSuccess) return st;

@@ -43,12 +43,35 @@ struct PrefillGemmArgs {
     uint32_t* amax;              // KIND 0: per sorted row max |a| (float bits), zeroed before
     int out_ld;                  // I (KIND 0) or H (KIND 1)
     int32_t* err;                // optional error word (bit 1: a bounded wait gave up)
+    int a_rows;                  // rows of the A matrix: T (KIND 0) or P (KIND 1)
+    int experts;                 // E
 };
+
+// Prescale of one (expert, 128-row weight block) scale row: f16x2 splats of scale * 2^p per
+// 128-wide K block into tbl (if non-null) and 2^-p returned, with 2^p chosen so that 448 * scale
+// * 2^p stays below 2^15. One warp.
+__device__ __forceinline__ float weight_prescale(const float* srow, int KB, uint32_t* tbl) {
+    const int lane = threadIdx.x & 31;
+    float m = 0.0f;
+    for (int kb = lane; kb < KB; kb += 32) m = fmaxf(m, fabsf(srow[kb]));
+    m = warp_max(m) * 448.0f;
+    float inv;
+    const float pre = pow2_range_scale(m, inv);
+    if (tbl != nullptr)
+        for (int kb = lane; kb < KB; kb += 32) {
+            const __half h = __float2half_rn(srow[kb] * pre);
+            tbl[kb] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&h)) * 0x10001u;
+        }
+    return inv;
+}
 
 // Launch one grouped GEMM (KIND 0: gate/up + SwiGLU, KIND 1: down) on the simple tcgen05 core
 // (prefill_tc.cu) or the warp-specialised one (prefill_ws.cu; N_total = I or H, it picks its own
 // column tiling and sets n_tiles).
 cudaError_t launch_prefill_gemm_tc(int kind, const PrefillGemmArgs& p, cudaStream_t stream);
 cudaError_t launch_prefill_gemm_ws(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
+// TMA-fed variant of the warp-specialised core (prefill_tma.cu): A and the E4M3 weight slices
+// arrive by tensor-map copies (a row gather for the gate/up activations).
+cudaError_t launch_prefill_gemm_tma(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
 
 }  // namespace moe

@@ -42,24 +42,6 @@ struct WsCfg {
     static_assert(kStage % 1024 == 0 && (kWsA + kRaw) % 1024 == 0, "stage alignment");
 };
 
-// Prescale of one (expert, 128-row weight block) scale row: f16x2 splats of scale * 2^p per
-// 128-wide K block into tbl (if non-null) and 2^-p returned, with 2^p chosen so that 448 * scale
-// * 2^p stays below 2^15. One warp.
-__device__ __forceinline__ float weight_prescale(const float* srow, int KB, uint32_t* tbl) {
-    const int lane = threadIdx.x & 31;
-    float m = 0.0f;
-    for (int kb = lane; kb < KB; kb += 32) m = fmaxf(m, fabsf(srow[kb]));
-    m = warp_max(m) * 448.0f;
-    float inv;
-    const float pre = pow2_range_scale(m, inv);
-    if (tbl != nullptr)
-        for (int kb = lane; kb < KB; kb += 32) {
-            const __half h = __float2half_rn(srow[kb] * pre);
-            tbl[kb] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&h)) * 0x10001u;
-        }
-    return inv;
-}
-
 }  // namespace
 
 template <int KIND, int BN>
@@ -105,22 +87,31 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_gemm_kernel(const Pr
 
     if (tid < kProdThreads) {
         // ---------------- producers ----------------
+        // Lane l of warp w copies 16-byte chunk (l >> 3) (+4) of rows 8g + (l & 7): each warp
+        // instruction reads whole 64-byte row segments (coalesced) and its eight-lane phases write
+        // eight distinct shared-memory bank groups (conflict-free in both layouts).
+        const int rr = tid & 7, cc = (tid >> 3) & 3, w = tid >> 5;
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
             const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
             const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
             const int rows = min(128, p.offsets[e + 1] - r0);
-            const int r = r0 + min(tid, rows - 1);           // padded rows repeat the last valid row
-            const __half* arow = KIND == 0 ? p.a + static_cast<size_t>(p.sorted_pair[r] / p.topk) * K
-                                           : p.a + static_cast<size_t>(r) * K;
-            const uint8_t* brow[2];
+            const __half* asrc[4];                            // A rows 8 * (4w + j) + rr
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int n = tid + 128 * j;
+            for (int j = 0; j < 4; ++j) {
+                const int r = r0 + min(8 * (4 * w + j) + rr, rows - 1);   // padded rows repeat the last
+                asrc[j] = (KIND == 0 ? p.a + static_cast<size_t>(p.sorted_pair[r] / p.topk) * K
+                                     : p.a + static_cast<size_t>(r) * K) + cc * 8;
+            }
+            const uint8_t* bsrc[BN / 32];                     // weight rows 8 * (w + 4i) + rr
+#pragma unroll
+            for (int i = 0; i < BN / 32; ++i) {
+                const int n = 8 * (w + 4 * i) + rr;
                 if (KIND == 0)                                // rows 0..127 gate, 128..255 up
-                    brow[j] = (j == 0 ? p.w0 : p.w1) + (static_cast<size_t>(e) * p.wrows + nt * 128 + tid) * K;
+                    bsrc[i] = (n < 128 ? p.w0 : p.w1) + (static_cast<size_t>(e) * p.wrows + nt * 128 + (n & 127)) * K;
                 else
-                    brow[j] = p.w0 + (static_cast<size_t>(e) * p.wrows + nt * BN + (n < BN ? n : 0)) * K;
+                    bsrc[i] = p.w0 + (static_cast<size_t>(e) * p.wrows + nt * BN + n) * K;
+                bsrc[i] += cc * 16;
             }
             for (int kt = 0; kt < KT; ++kt, ++sc) {
                 const uint32_t s = sc % NS, u = sc / NS;
@@ -128,15 +119,15 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_gemm_kernel(const Pr
                     abort_s = 1;
                     break;
                 }
-                uint8_t* dA = stA(s) + (tid >> 3) * 1024 + (tid & 7) * 16;
+                uint8_t* dA = stA(s) + (4 * w) * 1024 + cc * 128 + rr * 16;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) cp_async16(dA + q * 128, arow + kt * 64 + q * 8);
-#pragma unroll
-                for (int j = 0; j < BN / 128; ++j) {
-                    uint8_t* dR = stRaw(s) + (tid + 128 * j) * kWsRawRow;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) cp_async16(dR + q * 16, brow[j] + kt * 64 + q * 16);
+                for (int j = 0; j < 4; ++j) {
+                    cp_async16(dA + j * 1024, asrc[j] + kt * 64);
+                    cp_async16(dA + j * 1024 + 512, asrc[j] + kt * 64 + 32);
                 }
+                uint8_t* dR = stRaw(s) + (8 * w + rr) * kWsRawRow + cc * 16;
+#pragma unroll
+                for (int i = 0; i < BN / 32; ++i) cp_async16(dR + i * 32 * kWsRawRow, bsrc[i] + kt * 64);
                 cp_async_mbar_arrive(&full[s]);
             }
         }

@@ -65,6 +65,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzled layout that a TMA
+// load with 128-byte swizzle writes: rows of 128 bytes, 8-row groups 1024 bytes apart (stride
+// offset), leading offset unused, layout type 2 (bits 61-63). The group must be 1024-byte aligned;
+// a K step inside the 128-byte row advances the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16 (bits 7-9, 10-12 = 0),
 // both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 template <int M, int N>
@@ -109,6 +122,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* m) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
                  ::"r"(smem_u32(m)) : "memory");
+}
+
+// Arrive on m and raise its expected transaction byte count by tx (for TMA loads that complete on m).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* m, uint32_t tx) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(smem_u32(m)), "r"(tx) : "memory");
+}
+
+// TMA: box (x, y) of the 2-D tensor map into shared memory, completing tx bytes on m.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(m)) : "memory");
+}
+
+// TMA gather: columns x.. (the map's one-row box width) of rows y0..y3, stored as four consecutive
+// box rows at dst, completing tx bytes on m.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int y0, int y1, int y2,
+                                            int y3, uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+          "r"(smem_u32(m)) : "memory");
 }
 
 // Arrive on m once every cp.async previously issued by this thread has landed (count not raised).

@@ -53,7 +53,7 @@ size_t fused_smem_bytes(int H, int rows, int topk, int cap);
 
 // Wide tier (prefill.cu): workspace layout and the launch sequence of the grouped-GEMM path.
 struct PrefillLayout {
-    size_t counts, offsets, sorted_pair, pair_to_sorted, tiles, tile_e, tile_r0;
+    size_t counts, offsets, sorted_pair, pair_to_sorted, tiles, tile_e, tile_r0, tile_first, tile_cnt;
     size_t x16, xinv, amax, a16, ainv, f32, total;
 };
 PrefillLayout prefill_layout(int T, int H, int I, int E, int topk);

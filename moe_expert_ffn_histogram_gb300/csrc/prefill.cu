@@ -36,12 +36,15 @@ namespace moe {
 // ---- tile list -----------------------------------------------------------------------------------
 
 // One block: m-tile list from the per-expert counts (ascending expert, 128 sorted rows per tile).
-// tiles[0] = number of m-tiles; tile_e[i], tile_r0[i] = expert and first sorted row of tile i.
+// tiles[0] = number of m-tiles; tile_e[i], tile_r0[i] = expert and first sorted row of tile i;
+// tile_first[i], tile_cnt[i] = first m-tile and number of m-tiles of that expert.
 __global__ void __launch_bounds__(1024) prefill_tiles_kernel(const int32_t* __restrict__ counts,
                                                              const int32_t* __restrict__ offsets,
                                                              int E, int32_t* __restrict__ tiles,
                                                              int32_t* __restrict__ tile_e,
-                                                             int32_t* __restrict__ tile_r0) {
+                                                             int32_t* __restrict__ tile_r0,
+                                                             int32_t* __restrict__ tile_first,
+                                                             int32_t* __restrict__ tile_cnt) {
     __shared__ int warp_sum[32];
     __shared__ int base_s;
     if (threadIdx.x == 0) base_s = 0;
@@ -73,6 +76,8 @@ __global__ void __launch_bounds__(1024) prefill_tiles_kernel(const int32_t* __re
         for (int i = 0; i < n; ++i) {
             tile_e[start + i] = e;
             tile_r0[start + i] = offsets[e] + i * prefill::kBM;
+            tile_first[start + i] = start;
+            tile_cnt[start + i] = n;
         }
         __syncthreads();
         if (threadIdx.x == blockDim.x - 1) base_s = start + n;
@@ -384,6 +389,8 @@ PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     L.tiles = take(16);
     L.tile_e = take(mtiles * 4);
     L.tile_r0 = take(mtiles * 4);
+    L.tile_first = take(mtiles * 4);
+    L.tile_cnt = take(mtiles * 4);
     L.x16 = take(static_cast<size_t>(T) * H * 2);
     L.xinv = take(static_cast<size_t>(T) * 4);
     L.amax = take(P * 4);
@@ -419,7 +426,8 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
                                 stream)) != cudaSuccess)
         return st;
     prefill_tiles_kernel<<<1, 1024, 0, stream>>>(I32(L.counts), I32(L.offsets), E, I32(L.tiles),
-                                                 I32(L.tile_e), I32(L.tile_r0));
+                                                 I32(L.tile_e), I32(L.tile_r0), I32(L.tile_first),
+                                                 I32(L.tile_cnt));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
     float* xinv = reinterpret_cast<float*>(ws + L.xinv);
@@ -441,6 +449,8 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     gu.tiles = I32(L.tiles);
     gu.tile_e = I32(L.tile_e);
     gu.tile_r0 = I32(L.tile_r0);
+    gu.tile_first = I32(L.tile_first);
+    gu.tile_cnt = I32(L.tile_cnt);
     gu.offsets = I32(L.offsets);
     gu.sorted_pair = I32(L.sorted_pair);
     gu.topk = topk;

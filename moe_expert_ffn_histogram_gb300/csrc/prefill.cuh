@@ -25,6 +25,8 @@ struct PrefillGemmArgs {
     const int32_t* tiles;        // [1] number of m-tiles
     const int32_t* tile_e;       // [m-tiles]
     const int32_t* tile_r0;      // [m-tiles]
+    const int32_t* tile_first;   // [m-tiles] first m-tile of the tile's expert
+    const int32_t* tile_cnt;     // [m-tiles] number of m-tiles of the tile's expert
     const int32_t* offsets;      // [E+1]
     const int32_t* sorted_pair;  // [P]
     int topk, K, n_tiles;
@@ -46,6 +48,17 @@ struct PrefillGemmArgs {
     int a_rows;                  // rows of the A matrix: T (KIND 0) or P (KIND 1)
     int experts;                 // E
 };
+
+// (m-tile, n-tile) of work item `tile` in expert-major, n-tile-middle, m-tile-minor order: the
+// CTAs running at one time share few weight slabs (each slab is read from HBM about once and
+// served to the expert's m-tiles from L2) while the expert's activation rows stay in L2.
+__device__ __forceinline__ void decode_tile(const PrefillGemmArgs& p, int tile, int& mt, int& nt) {
+    const int m = tile / p.n_tiles;
+    const int first = p.tile_first[m], cnt = p.tile_cnt[m];
+    const int local = tile - p.n_tiles * first;
+    nt = local / cnt;
+    mt = first + (local - nt * cnt);
+}
 
 // Prescale of one (expert, 128-row weight block) scale row: f16x2 splats of scale * 2^p per
 // 128-wide K block into tbl (if non-null) and 2^-p returned, with 2^p chosen so that 448 * scale

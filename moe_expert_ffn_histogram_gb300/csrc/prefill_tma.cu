@@ -2,15 +2,16 @@
 //
 // Tiles, tile list and epilogues are those of prefill_ws.cu; what changes is how operands reach
 // shared memory, which there cost one cp.async per 16 bytes per thread and bounded the kernel:
-//   warp 0      producer   one lane arms full[s] with the slice's byte count, then TMA copies
+//   warps 0-3   producers  warp w owns load stage w: one lane arms full[w] with the slice's byte
+//                          count, then TMA copies
 //                          land the A slice (gate/up: 32 four-row gathers of x16 rows by token,
 //                          one per lane; down: one 128-row box of a16) in the 128-byte swizzled
 //                          K-major layout the MMA reads directly, and the E4M3 weight slice (one
 //                          or two 128-row boxes, 64-byte swizzled) - four load stages deep;
-//   warps 1-8   converters dequantise weight slice s to f16 x prescaled block scale into one of
+//   warps 4-11  converters dequantise weight slice s to f16 x prescaled block scale into one of
 //                          two B buffers (canonical no-swizzle K-major), fence, arrive bfull[b];
-//   warps 9-12  epilogue   as in prefill_ws.cu (warp w reads TMEM lanes 32*(w%4) .. +31);
-//   warp 13     MMA        one thread: four M=128 x N=BN x K=16 tcgen05.mma per slice into one of
+//   warps 12-15 epilogue   as in prefill_ws.cu (warp w reads TMEM lanes 32*(w%4) .. +31);
+//   warp 16     MMA        one thread: four M=128 x N=BN x K=16 tcgen05.mma per slice into one of
 //                          two TMEM accumulators; commits free the load stage, the B buffer and,
 //                          after a tile's last slice, hand the accumulator to the epilogue.
 // Every wait is bounded (~1 s of SM clock); on a timeout the CTA sets bit 1 of the error word,
@@ -28,13 +29,14 @@ namespace {
 constexpr int kTmLoadStages = 4;                 // A + raw weight slices in flight
 constexpr int kTmBStages = 2;                    // converted weight slices
 constexpr int kTmA = 128 * 128;                  // A slice: 128 rows x 64 f16, 128B-swizzled (16 KB)
+constexpr int kTmProdWarps = kTmLoadStages;     // producer warp w owns load stage w
 constexpr int kTmConvWarps = 8;
 constexpr int kTmConvThreads = 32 * kTmConvWarps;
 constexpr int kTmEpiThreads = 128;
-constexpr int kTmConvWarp0 = 1;
-constexpr int kTmEpiWarp0 = kTmConvWarp0 + kTmConvWarps;   // 9
-constexpr int kTmMmaWarp = kTmEpiWarp0 + 4;                // 13
-constexpr int kTmThreads = 32 * (kTmMmaWarp + 1);          // 448
+constexpr int kTmConvWarp0 = kTmProdWarps;                 // 4
+constexpr int kTmEpiWarp0 = kTmConvWarp0 + kTmConvWarps;   // 12
+constexpr int kTmMmaWarp = kTmEpiWarp0 + 4;                // 16
+constexpr int kTmThreads = 32 * (kTmMmaWarp + 1);          // 544
 
 template <int BN>
 struct TmCfg {
@@ -94,11 +96,14 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    if (warp == 0) {
-        // ---------------- producer ----------------
+    if (warp < kTmProdWarps) {
+        // ---------------- producers ----------------
+        // A TMA issue costs the issuing thread tens to hundreds of cycles; four warps, each
+        // owning one load stage (slices sc with sc % 4 == warp), keep the copies flowing.
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
-            const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+            int mt, nt;
+            decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
             const int rows = min(128, p.offsets[e + 1] - r0);
             int g[4] = {0, 0, 0, 0};                       // this lane's four A rows (gate/up): tokens
@@ -111,6 +116,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             const int wy1 = KIND == 0 ? wy0 : wy0 + 128;
             for (int kt = 0; kt < KT; ++kt, ++sc) {
                 const uint32_t s = sc % NL, u = sc / NL;
+                if (static_cast<int>(s) != warp) continue;
                 if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(&empty[s], (u - 1) & 1u))) {
                     abort_s = 1;
                     break;
@@ -137,7 +143,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         uint32_t* tbl = w_scale[cw];
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
-            const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+            int mt, nt;
+            decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt];
             __syncwarp();                                  // the old table is no longer read
             const size_t sblk = static_cast<size_t>(e) * (p.wrows / 128);
@@ -219,7 +226,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         const int row = 32 * q + lane;
         uint32_t tcount = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x, ++tcount) {
-            const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+            int mt, nt;
+            decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
             const int rows = min(128, p.offsets[e + 1] - r0);
             const int rr = r0 + min(row, rows - 1);
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                                     : winv[0];
             }
             const uint32_t b = tcount & 1u, v = tcount >> 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[b], v & 1u))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(&acc_full[b], v & 1u))) {
                 abort_s = 1;
                 break;
             }

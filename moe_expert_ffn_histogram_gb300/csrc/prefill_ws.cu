@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_gemm_kernel(const Pr
         const int rr = tid & 7, cc = (tid >> 3) & 3, w = tid >> 5;
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
-            const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+            int mt, nt;
+            decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
             const int rows = min(128, p.offsets[e + 1] - r0);
             const __half* asrc[4];                            // A rows 8 * (4w + j) + rr
@@ -139,7 +140,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_gemm_kernel(const Pr
         const int ct = tid - kProdThreads, cw = ct >> 5;
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
-            const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+            int mt, nt;
+            decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt];
             __syncwarp();                                     // the old tables are no longer read
             const size_t sblk = static_cast<size_t>(e) * (p.wrows / 128);
@@ -226,7 +228,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_gemm_kernel(const Pr
         const int row = 32 * q + lane;
         uint32_t tcount = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x, ++tcount) {
-            const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+            int mt, nt;
+            decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
             const int rows = min(128, p.offsets[e + 1] - r0);
             const int rr = r0 + min(row, rows - 1);
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) prefill_ws_gemm_kernel(const Pr
                                     : winv[0];
             }
             const uint32_t b = tcount & 1u, v = tcount >> 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[b], v & 1u))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(&acc_full[b], v & 1u))) {
                 abort_s = 1;
                 break;
             }

@@ -16,20 +16,34 @@ __device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_test(uint64_t* m, uint32_t parity) {
+// One try_wait on the phase of parity `parity`: the thread may be suspended in hardware until the
+// phase completes or about hint_ns nanoseconds pass, so a waiting warp takes few issue slots.
+__device__ __forceinline__ bool mbar_test(uint64_t* m, uint32_t parity, uint32_t hint_ns = 20000) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(smem_u32(m)), "r"(parity) : "memory");
+        : "=r"(ok) : "r"(smem_u32(m)), "r"(parity), "r"(hint_ns) : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase of parity `parity` of mbarrier m; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity) {
+    if (mbar_test(m, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_test(m, parity))
         if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// The same for a wait that is off the critical path (a whole tile long): sleeps between tries.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* m, uint32_t parity) {
+    if (mbar_test(m, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(m, parity)) {
+        __nanosleep(256);
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
     return true;
 }
 

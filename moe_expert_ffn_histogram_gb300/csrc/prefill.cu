@@ -88,10 +88,15 @@ __global__ void __launch_bounds__(1024) prefill_tiles_kernel(const int32_t* __re
 
 // ---- x prep ---------------------------------------------------------------------------------------
 
-// One block per token: x16[t] = f16(x[t] * s_t), xinv[t] = 1 / s_t, s_t a power of two.
+// One block per token: x16[t] = f16(x[t] * s_t), xinv[t] = 1 / s_t, s_t a power of two. With
+// pair_to_sorted given, the row is instead written to each of the token's topk sorted rows of
+// x16 (then [P][H]; pairs marked -1 are skipped), so that the gate/up GEMM reads its A tiles as
+// plain boxes.
 __global__ void __launch_bounds__(256) prefill_x_prep_kernel(const __nv_bfloat16* __restrict__ x,
                                                              int H, __half* __restrict__ x16,
-                                                             float* __restrict__ xinv) {
+                                                             float* __restrict__ xinv,
+                                                             const int32_t* __restrict__ pair_to_sorted,
+                                                             int topk) {
     __shared__ float red[8];
     const int t = blockIdx.x, tid = threadIdx.x;
     const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(256) prefill_x_prep_kernel(const __nv_bfloat16
     float inv;
     const float s = pow2_range_scale(mm, inv);
     if (tid == 0) xinv[t] = inv;
-    uint4* dst = reinterpret_cast<uint4*>(x16 + static_cast<size_t>(t) * H);
+    const int ncopy = pair_to_sorted != nullptr ? topk : 1;
     for (int v = tid; v < nv; v += 256) {
         const uint4 q = __ldg(xr + v);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -126,7 +131,11 @@ __global__ void __launch_bounds__(256) prefill_x_prep_kernel(const __nv_bfloat16
                                                  __uint_as_float(w[i] & 0xFFFF0000u) * s);
             o[i] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int c = 0; c < ncopy; ++c) {
+            const int row = pair_to_sorted != nullptr ? pair_to_sorted[static_cast<size_t>(t) * topk + c] : t;
+            if (row < 0) continue;                            // pair with an out-of-range expert id
+            reinterpret_cast<uint4*>(x16 + static_cast<size_t>(row) * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
     }
 }
 
@@ -391,7 +400,7 @@ PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     L.tile_r0 = take(mtiles * 4);
     L.tile_first = take(mtiles * 4);
     L.tile_cnt = take(mtiles * 4);
-    L.x16 = take(static_cast<size_t>(T) * H * 2);
+    L.x16 = take((MOE_PREFILL_TC == 3 ? P : static_cast<size_t>(T)) * H * 2);   // [P][H] sorted for TMA
     L.xinv = take(static_cast<size_t>(T) * 4);
     L.amax = take(P * 4);
     L.a16 = take(P * static_cast<size_t>(I) * 2);
@@ -431,7 +440,8 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
     float* xinv = reinterpret_cast<float*>(ws + L.xinv);
-    prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv);
+    prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv,
+                                                  MOE_PREFILL_TC == 3 ? I32(L.pair_to_sorted) : nullptr, topk);
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
     if ((st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess) return st;
@@ -468,7 +478,7 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     gu.amax = amax;
     gu.out_ld = I;
     gu.err = err;
-    gu.a_rows = T;
+    gu.a_rows = MOE_PREFILL_TC == 3 ? P : T;
     gu.experts = E;
     if (MOE_PREFILL_TC == 3) {
         if ((st = launch_prefill_gemm_tma(0, gu, I, stream)) != cudaSuccess) return st;

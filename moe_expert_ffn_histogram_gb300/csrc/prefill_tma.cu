@@ -1,21 +1,22 @@
-// TMA-fed warp-specialised tcgen05 core of the prefill grouped GEMMs.
+// TMA-fed warp-specialised tcgen05 core of the prefill grouped GEMMs (the default prefill core).
 //
-// Tiles, tile list and epilogues are those of prefill_ws.cu; what changes is how operands reach
-// shared memory, which there cost one cp.async per 16 bytes per thread and bounded the kernel:
-//   warps 0-3   producers  warp w owns load stage w: one lane arms full[w] with the slice's byte
-//                          count, then TMA copies
-//                          land the A slice (gate/up: 32 four-row gathers of x16 rows by token,
-//                          one per lane; down: one 128-row box of a16) in the 128-byte swizzled
-//                          K-major layout the MMA reads directly, and the E4M3 weight slice (one
-//                          or two 128-row boxes, 64-byte swizzled) - four load stages deep;
-//   warps 4-11  converters dequantise weight slice s to f16 x prescaled block scale into one of
-//                          two B buffers (canonical no-swizzle K-major), fence, arrive bfull[b];
-//   warps 12-15 epilogue   as in prefill_ws.cu (warp w reads TMEM lanes 32*(w%4) .. +31);
-//   warp 16     MMA        one thread: four M=128 x N=BN x K=16 tcgen05.mma per slice into one of
+// Tiles and epilogues are those of prefill_ws.cu; what changes is how operands reach shared
+// memory (there one cp.async per 16 bytes per thread, which bounded the kernel) and how the
+// weight conversion overlaps:
+//   warps 0-2   producers  warp w owns load stage w: one thread arms full[w] with the slice's
+//                          byte count and issues three TMA boxes - 128 sorted rows x 64 f16 of A
+//                          (128-byte swizzle: the K-major layout the MMA reads directly) and the
+//                          slice's E4M3 weight rows (64-byte swizzle);
+//   warps 3-10  converters two groups of four warps take alternate slices: dequantise the weight
+//                          slice to f16 x prescaled block scale into B buffer sc % 3 (canonical
+//                          no-swizzle K-major), fence the async proxy, arrive bfull;
+//   warps 11-14 epilogue   as in prefill_ws.cu (warp w reads TMEM lanes 32*(w%4) .. +31);
+//   warp 15     MMA        one thread: four M=128 x N=BN x K=16 tcgen05.mma per slice into one of
 //                          two TMEM accumulators; commits free the load stage, the B buffer and,
 //                          after a tile's last slice, hand the accumulator to the epilogue.
-// Every wait is bounded (~1 s of SM clock); on a timeout the CTA sets bit 1 of the error word,
-// every role leaves its loop, and the CTA frees its TMEM and exits.
+// Gate/up reads A from the sorted copy of x16 that the x prep kernel writes ([P][H]); down reads
+// a16 ([P][I]). Every wait is bounded (~1 s of SM clock); on a timeout the CTA sets bit 1 of the
+// error word, every role leaves its loop, and the CTA frees its TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -26,24 +27,26 @@ namespace moe {
 
 namespace {
 
-constexpr int kTmLoadStages = 4;                 // A + raw weight slices in flight
-constexpr int kTmBStages = 2;                    // converted weight slices
+constexpr int kTmStages = 3;                     // load stages = converted-weight buffers: slice sc
+                                                 // uses load stage and B buffer sc % 3
 constexpr int kTmA = 128 * 128;                  // A slice: 128 rows x 64 f16, 128B-swizzled (16 KB)
-constexpr int kTmProdWarps = kTmLoadStages;     // producer warp w owns load stage w
-constexpr int kTmConvWarps = 8;
-constexpr int kTmConvThreads = 32 * kTmConvWarps;
+constexpr int kTmProdWarps = kTmStages;          // producer warp w owns load stage w
+constexpr int kTmConvGroups = 2;                 // converter group g takes slices sc % 2 == g
+constexpr int kTmGroupWarps = 4;
+constexpr int kTmGroupThreads = 32 * kTmGroupWarps;
+constexpr int kTmConvWarps = kTmConvGroups * kTmGroupWarps;
 constexpr int kTmEpiThreads = 128;
-constexpr int kTmConvWarp0 = kTmProdWarps;                 // 4
-constexpr int kTmEpiWarp0 = kTmConvWarp0 + kTmConvWarps;   // 12
-constexpr int kTmMmaWarp = kTmEpiWarp0 + 4;                // 16
-constexpr int kTmThreads = 32 * (kTmMmaWarp + 1);          // 544
+constexpr int kTmConvWarp0 = kTmProdWarps;                 // 3
+constexpr int kTmEpiWarp0 = kTmConvWarp0 + kTmConvWarps;   // 11
+constexpr int kTmMmaWarp = kTmEpiWarp0 + 4;                // 15
+constexpr int kTmThreads = 32 * (kTmMmaWarp + 1);          // 512
 
 template <int BN>
 struct TmCfg {
     static constexpr int kRaw = BN * 64;                   // raw E4M3 slice, 64B-swizzled rows
     static constexpr int kLoad = kTmA + kRaw;              // one load stage
     static constexpr int kB = BN * 128;                    // converted f16 slice
-    static constexpr int kSmem = kTmLoadStages * kLoad + kTmBStages * kB + 1024;
+    static constexpr int kSmem = kTmStages * (kLoad + kB) + 1024;
     static constexpr uint32_t kTmemCols = 2 * BN;          // two fp32 accumulators
     static_assert(kLoad % 1024 == 0 && kB % 1024 == 0, "stage alignment");
 };
@@ -55,12 +58,12 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     prefill_tma_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1) {
     using Cfg = TmCfg<BN>;
-    constexpr int NL = kTmLoadStages, NB = kTmBStages;
+    constexpr int NL = kTmStages, NB = kTmStages;
     constexpr uint32_t kIdescN = idesc_f16_f32<128, BN>();
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[NL], empty[NL], bfull[NB], bempty[NB], acc_full[2], acc_empty[2];
-    __shared__ uint32_t w_scale[kTmConvWarps][64];       // per converter warp: one scale table
+    __shared__ uint32_t w_scale[kTmConvWarps][2][64];    // per converter warp: the tile's two tables
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
 
@@ -77,7 +80,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < NB; ++b) {
-            mbar_init(&bfull[b], kTmConvThreads);
+            mbar_init(&bfull[b], kTmGroupWarps);
             mbar_init(&bempty[b], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -98,76 +101,80 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 
     if (warp < kTmProdWarps) {
         // ---------------- producers ----------------
-        // A TMA issue costs the issuing thread tens to hundreds of cycles; four warps, each
-        // owning one load stage (slices sc with sc % 4 == warp), keep the copies flowing.
-        uint32_t sc = 0;
-        for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
-            int mt, nt;
-            decode_tile(p, tile, mt, nt);
-            const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
-            const int rows = min(128, p.offsets[e + 1] - r0);
-            int g[4] = {0, 0, 0, 0};                       // this lane's four A rows (gate/up): tokens
-            if (KIND == 0) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)                // padded rows repeat the last valid row
-                    g[j] = p.sorted_pair[r0 + min(4 * lane + j, rows - 1)] / p.topk;
-            }
-            const int wy0 = e * p.wrows + (KIND == 0 ? nt * 128 : nt * BN);
-            const int wy1 = KIND == 0 ? wy0 : wy0 + 128;
-            for (int kt = 0; kt < KT; ++kt, ++sc) {
-                const uint32_t s = sc % NL, u = sc / NL;
-                if (static_cast<int>(s) != warp) continue;
-                if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(&empty[s], (u - 1) & 1u))) {
-                    abort_s = 1;
-                    break;
-                }
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], kTmA + Cfg::kRaw);
-                __syncwarp();
-                const uint32_t a_dst = smem_u32(stA(s)), r_dst = smem_u32(stRaw(s));
-                if (KIND == 0)
-                    tma_gather4(a_dst + lane * 512, &tmA, kt * 64, g[0], g[1], g[2], g[3], &full[s]);
-                if (lane == 0) {
-                    if (KIND == 1) tma_load_2d(a_dst, &tmA, kt * 64, r0, &full[s]);
+        // A TMA issue costs the issuing thread tens to hundreds of cycles; three warps, each
+        // owning one load stage (slices sc with sc % 3 == warp), keep the copies flowing.
+        if (lane == 0) {
+            uint32_t sc = 0;
+            for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
+                int mt, nt;
+                decode_tile(p, tile, mt, nt);
+                const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
+                const int wy0 = e * p.wrows + (KIND == 0 ? nt * 128 : nt * BN);
+                const int wy1 = KIND == 0 ? wy0 : wy0 + 128;
+                bool ok = true;
+                for (int kt = 0; kt < KT; ++kt, ++sc) {
+                    const uint32_t s = sc % NL, u = sc / NL;
+                    if (static_cast<int>(s) != warp) continue;
+                    if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], kTmA + Cfg::kRaw);
+                    const uint32_t a_dst = smem_u32(stA(s)), r_dst = smem_u32(stRaw(s));
+                    tma_load_2d(a_dst, &tmA, kt * 64, r0, &full[s]);   // rows past the expert: unused
                     tma_load_2d(r_dst, &tmW0, kt * 64, wy0, &full[s]);
                     if (BN == 256) tma_load_2d(r_dst + 128 * 64, KIND == 0 ? &tmW1 : &tmW0, kt * 64, wy1, &full[s]);
+                }
+                if (!ok) {
+                    abort_s = 1;
+                    break;
                 }
             }
         }
     } else if (warp < kTmEpiWarp0) {
         // ---------------- converters ----------------
-        // Work item i = ct + 256 j is the 16-byte raw chunk q = i / BN of weight row n = i % BN:
-        // eight consecutive lanes take eight consecutive rows of one chunk, which the 64-byte
-        // swizzle spreads over eight bank groups for the reads, as (n & 7) does for the writes.
+        // Two groups of four warps take alternate slices, so one slice's conversion overlaps the
+        // next. Work item i = gt + 128 j of a slice is the 16-byte raw chunk q = i / BN of weight
+        // row n = i % BN: eight consecutive lanes take eight consecutive rows of one chunk, which
+        // the 64-byte swizzle spreads over eight bank groups for the reads, as (n & 7) does for
+        // the writes. A slice waits first for its B buffer (whose previous slice, three back,
+        // the MMA has then consumed) and only then for its load stage, so that parity waits
+        // never run two phases ahead.
         const int ct = tid - 32 * kTmConvWarp0, cw = ct >> 5;
-        const int half = BN == 256 ? (cw >= kTmConvWarps / 2) : 0;   // rows of this warp: 0..127 or 128..
-        uint32_t* tbl = w_scale[cw];
+        const int grp = cw / kTmGroupWarps, gt = ct % kTmGroupThreads;
+        uint32_t(*tbl)[64] = w_scale[cw];
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
             int mt, nt;
             decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt];
-            __syncwarp();                                  // the old table is no longer read
+            __syncwarp();                                  // the old tables are no longer read
             const size_t sblk = static_cast<size_t>(e) * (p.wrows / 128);
-            if (KIND == 0)
-                weight_prescale((half ? p.s1 : p.s0) + (sblk + nt) * KB, KB, tbl);
-            else
-                weight_prescale(p.s0 + (sblk + (nt * BN) / 128 + half) * KB, KB, tbl);
+            if (KIND == 0) {                               // rows 0..127 gate, 128..255 up
+                weight_prescale(p.s0 + (sblk + nt) * KB, KB, tbl[0]);
+                weight_prescale(p.s1 + (sblk + nt) * KB, KB, tbl[1]);
+            } else {                                       // rows 128.. in the next 128-row block
+                weight_prescale(p.s0 + (sblk + (nt * BN) / 128) * KB, KB, tbl[0]);
+                if (BN == 256) weight_prescale(p.s0 + (sblk + (nt * BN) / 128 + 1) * KB, KB, tbl[1]);
+            }
             __syncwarp();
+            bool ok = true;
             for (int kt = 0; kt < KT; ++kt, ++sc) {
-                const uint32_t s = sc % NL, u = sc / NL, b = sc % NB, ub = sc / NB;
-                bool ok = mbar_wait(&full[s], u & 1u);
-                if (ok && ub > 0) ok = mbar_wait(&bempty[b], (ub - 1) & 1u);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    abort_s = 1;
+                if (static_cast<int>(sc % kTmConvGroups) != grp) continue;
+                const uint32_t s = sc % NL, u = sc / NL;
+                bool w_ok = u == 0 || mbar_wait(&bempty[s], (u - 1) & 1u);
+                if (w_ok) w_ok = mbar_wait(&full[s], u & 1u);
+                if (!__all_sync(0xffffffffu, w_ok)) {
+                    ok = false;
                     break;
                 }
-                const uint32_t sc2 = tbl[kt >> 1];
                 const uint8_t* raw = stRaw(s);
-                uint8_t* dst = stB(b);
+                uint8_t* dst = stB(s);
 #pragma unroll
-                for (int j = 0; j < BN * 4 / kTmConvThreads; ++j) {
-                    const int item = ct + kTmConvThreads * j;
+                for (int j = 0; j < BN * 4 / kTmGroupThreads; ++j) {
+                    const int item = gt + kTmGroupThreads * j;
                     const int n = item % BN, q = item / BN;
+                    const uint32_t sc2 = tbl[n >> 7][kt >> 1];
                     const uint4 w = lds128(raw + n * 64 + ((q ^ ((n >> 1) & 3)) << 4));
                     const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
                     uint32_t h[8];
@@ -182,7 +189,12 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                     *reinterpret_cast<uint4*>(dB + 128) = make_uint4(h[4], h[5], h[6], h[7]);
                 }
                 fence_async_smem();                        // B visible to the MMA (async proxy)
-                mbar_arrive(&bfull[b]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bfull[s]);
+            }
+            if (!ok) {
+                abort_s = 1;
+                break;
             }
         }
     } else if (warp == kTmMmaWarp) {
@@ -199,7 +211,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                 const uint32_t d = tmem + ab * BN;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt, ++sc) {
-                    const uint32_t s = sc % NL, u = sc / NL, b = sc % NB, ub = sc / NB;
+                    const uint32_t s = sc % NL, u = sc / NL, b = s, ub = u;
                     if (!mbar_wait(&full[s], u & 1u) || !mbar_wait(&bfull[b], ub & 1u)) {
                         ok = false;
                         break;
@@ -365,7 +377,7 @@ cudaError_t launch_prefill_gemm_tma(int kind, const PrefillGemmArgs& p, int N_to
     q.n_tiles = kind == 0 ? N_total / 128 : N_total / BN;
     CUtensorMap ma, mw0, mw1;
     const uint64_t wrows_all = static_cast<uint64_t>(p.experts) * p.wrows;
-    bool ok = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.a, p.K, p.a_rows, 64, kind == 0 ? 1 : 128,
+    bool ok = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.a, p.K, p.a_rows, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map_2d(&mw0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w0, p.K, wrows_all, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_64B) &&

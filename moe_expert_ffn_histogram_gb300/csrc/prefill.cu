@@ -23,11 +23,11 @@
 // fp32 epilogue. Products accumulate in fp32.
 #include "prefill.cuh"
 
-// Which grouped-GEMM core the prefill tier launches: 3 = TMA-fed warp-specialised tcgen05/TMEM
-// (prefill_tma.cu), 2 = cp.async-fed warp-specialised (prefill_ws.cu), 1 = simple tcgen05/TMEM
+// Which grouped-GEMM core the prefill tier launches: 4 = weights in TMEM (prefill_tw.cu),
+// 3 = TMA-fed warp-specialised tcgen05/TMEM (prefill_tma.cu), 2 = cp.async-fed warp-specialised (prefill_ws.cu), 1 = simple tcgen05/TMEM
 // (prefill_tc.cu), 0 = mma.sync (below).
 #ifndef MOE_PREFILL_TC
-#define MOE_PREFILL_TC 3
+#define MOE_PREFILL_TC 4
 #endif
 
 namespace moe {
@@ -400,7 +400,7 @@ PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     L.tile_r0 = take(mtiles * 4);
     L.tile_first = take(mtiles * 4);
     L.tile_cnt = take(mtiles * 4);
-    L.x16 = take((MOE_PREFILL_TC == 3 ? P : static_cast<size_t>(T)) * H * 2);   // [P][H] sorted for TMA
+    L.x16 = take((MOE_PREFILL_TC >= 3 ? P : static_cast<size_t>(T)) * H * 2);   // [P][H] sorted for TMA
     L.xinv = take(static_cast<size_t>(T) * 4);
     L.amax = take(P * 4);
     L.a16 = take(P * static_cast<size_t>(I) * 2);
@@ -441,7 +441,7 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
     float* xinv = reinterpret_cast<float*>(ws + L.xinv);
     prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv,
-                                                  MOE_PREFILL_TC == 3 ? I32(L.pair_to_sorted) : nullptr, topk);
+                                                  MOE_PREFILL_TC >= 3 ? I32(L.pair_to_sorted) : nullptr, topk);
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
     if ((st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess) return st;
@@ -478,9 +478,11 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     gu.amax = amax;
     gu.out_ld = I;
     gu.err = err;
-    gu.a_rows = MOE_PREFILL_TC == 3 ? P : T;
+    gu.a_rows = MOE_PREFILL_TC >= 3 ? P : T;
     gu.experts = E;
-    if (MOE_PREFILL_TC == 3) {
+    if (MOE_PREFILL_TC == 4) {
+        if ((st = launch_prefill_gemm_tw(0, gu, I, stream)) != cudaSuccess) return st;
+    } else if (MOE_PREFILL_TC == 3) {
         if ((st = launch_prefill_gemm_tma(0, gu, I, stream)) != cudaSuccess) return st;
     } else if (MOE_PREFILL_TC == 2) {
         if ((st = launch_prefill_gemm_ws(0, gu, I, stream)) != cudaSuccess) return st;
@@ -510,7 +512,9 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     dn.amax = nullptr;
     dn.out_ld = H;
     dn.a_rows = P;
-    if (MOE_PREFILL_TC == 3) {
+    if (MOE_PREFILL_TC == 4) {
+        if ((st = launch_prefill_gemm_tw(1, dn, H, stream)) != cudaSuccess) return st;
+    } else if (MOE_PREFILL_TC == 3) {
         if ((st = launch_prefill_gemm_tma(1, dn, H, stream)) != cudaSuccess) return st;
     } else if (MOE_PREFILL_TC == 2) {
         if ((st = launch_prefill_gemm_ws(1, dn, H, stream)) != cudaSuccess) return st;

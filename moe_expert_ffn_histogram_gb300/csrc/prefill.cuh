@@ -86,5 +86,7 @@ cudaError_t launch_prefill_gemm_ws(int kind, const PrefillGemmArgs& p, int N_tot
 // TMA-fed variant of the warp-specialised core (prefill_tma.cu): A and the E4M3 weight slices
 // arrive by tensor-map copies (a row gather for the gate/up activations).
 cudaError_t launch_prefill_gemm_tma(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
+// Transposed variant with the dequantised weights as the MMA's TMEM operand (prefill_tw.cu).
+cudaError_t launch_prefill_gemm_tw(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
 
 }  // namespace moe

@@ -170,13 +170,22 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                 }
                 const uint8_t* raw = stRaw(s);
                 uint8_t* dst = stB(s);
+                constexpr int kItems = BN * 4 / kTmGroupThreads;
+                // All of this slice's raw chunks are read before the first store, so the reads
+                // are not held behind stores the compiler cannot prove disjoint from them.
+                uint4 wr[kItems];
 #pragma unroll
-                for (int j = 0; j < BN * 4 / kTmGroupThreads; ++j) {
+                for (int j = 0; j < kItems; ++j) {
+                    const int item = gt + kTmGroupThreads * j;
+                    const int n = item % BN, q = item / BN;
+                    wr[j] = lds128(raw + n * 64 + ((q ^ ((n >> 1) & 3)) << 4));
+                }
+#pragma unroll
+                for (int j = 0; j < kItems; ++j) {
                     const int item = gt + kTmGroupThreads * j;
                     const int n = item % BN, q = item / BN;
                     const uint32_t sc2 = tbl[n >> 7][kt >> 1];
-                    const uint4 w = lds128(raw + n * 64 + ((q ^ ((n >> 1) & 3)) << 4));
-                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                    const uint32_t wv[4] = {wr[j].x, wr[j].y, wr[j].z, wr[j].w};
                     uint32_t h[8];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {

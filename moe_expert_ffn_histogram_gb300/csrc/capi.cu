@@ -55,6 +55,16 @@ int group_cap(int rows, int topk) {
     return cap < p ? cap : p;
 }
 
+// Columns per group in the fused kernel: its x staging is cap x H f16 of shared memory, and a cap
+// of 4 (57 KB at H = 7168) leaves room for two CTAs per SM. An expert picked by more tokens of
+// one sweep becomes several groups (its rows are then read once per group) - rare for sweeps of
+// <= 8 tokens over many experts.
+constexpr int kFusedCap = 4;
+int fused_cap(int rows, int topk) {
+    const int c = group_cap(rows, topk);
+    return c < kFusedCap ? c : kFusedCap;
+}
+
 int check_sizes(int T, int H, int I, int E, int topk) {
     if (!shape_ok(T, H, I, E, topk)) return MOE_ERR_SHAPE;
     const int rows = rows_per_sweep(T);
@@ -63,7 +73,8 @@ int check_sizes(int T, int H, int I, int E, int topk) {
     const int cap = rows == 1 ? 1 : group_cap(rows, topk);
     if (gate_up_smem_bytes(H, cap) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
     if (down_smem_bytes(rows, topk) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
-    if (fused_smem_bytes(H, rows, topk, cap) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    if (fused_smem_bytes(H, rows, topk, rows == 1 ? 1 : fused_cap(rows, topk)) > kMaxSmem)
+        return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -206,7 +217,7 @@ int stage_fused(const uint16_t* x, int rows, int H, int I, int E, int topk, cons
     da.act = ga.act;
     da.act_scale = ga.act_scale;
     da.out = reinterpret_cast<__nv_bfloat16*>(out);
-    const int cap = rows == 1 ? 1 : group_cap(rows, topk);
+    const int cap = rows == 1 ? 1 : fused_cap(rows, topk);
     return cuda_status(launch_fused_forward<FMT>(ga, da, w.at<unsigned>(w.L.barrier), rows, cap, s));
 }
 

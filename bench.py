@@ -399,7 +399,7 @@ def bench_ours(args):
                 "hbm_frac": round(mean_total / (ms * 1e-3) / 1e9 / peak, 4),
                 "note": "f16 x f16 -> f32 MMA, same nominal rate as bf16"}
         # route plan, tile list, x prep, gate/up GEMM, activation prep, down GEMM, combine
-        launches_per_step = 7 if c["fmt"] == "fp8" else ((T + 7) // 8)
+        launches_per_step = 7
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,

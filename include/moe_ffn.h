@@ -115,8 +115,13 @@ MOE_API int moe_route_permute(const int32_t* topk_ids, int T, int topk, int E, i
  *                 256-byte aligned.
  *
  * Arithmetic: weights decode exactly to f16, activations are carried as f16 with a power-of-two
- * scale per token (and per 64-wide block of the activation a), products accumulate in fp32, the
- * combine runs in slot order in fp32, and the result is rounded once to bf16.
+ * scale per token (and per 64-wide block, or per sorted row in the grouped-GEMM tier, of the
+ * activation a), products accumulate in fp32, the combine runs in slot order in fp32, and the
+ * result is rounded once to bf16.
+ *
+ * Tiers (chosen from the sizes alone): T == 1 two kernels; 2 <= T <= 8 one cooperative kernel; T > 8
+ * the grouped GEMM over expert-sorted rows on the tcgen05 tensor cores (H, I <= 8192, E <= 4096;
+ * the workspace then holds the sorted rows, ~P*(2H + 2I + 4*max(H,I)) bytes for P = T*topk).
  */
 MOE_API int moe_fp8_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
                     const int32_t* topk_ids, const float* topk_weights,
@@ -137,7 +142,8 @@ MOE_API int moe_fp8_forward(const uint16_t* x, int T, int H, int I, int E, int t
  *                 ("memra-engine 0.131.0 src/dsv4_ep.rs", `chain`: wstride = inter*hidden/2,
  *                 sstride = inter*hidden/16; "spark_model layers/glm5next_mlp/forward.rs",
  *                 `w4a16_gemv`: scale_2 is a by-value scalar).
- * Everything else as moe_fp8_forward.
+ * Everything else as moe_fp8_forward; the grouped-GEMM tier (T > 8) also needs H and I to be
+ * multiples of 256, otherwise T > 8 runs as sweeps of <= 8 tokens through the cooperative kernel.
  */
 MOE_API int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
                       const int32_t* topk_ids, const float* topk_weights,

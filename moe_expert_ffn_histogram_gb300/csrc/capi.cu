@@ -43,8 +43,10 @@ int rows_per_sweep(int T) { return T < kMaxRowsPerSweep ? T : kMaxRowsPerSweep; 
 // The grouped-GEMM (prefill) tier: FP8 weights, more than one 8-token sweep, and shapes its
 // tiles cover (per-K-block scale tables of <= 64 entries).
 bool uses_prefill(int T, int H, int I, int E, int fmt) {
-    return fmt == 0 && T > kMaxRowsPerSweep && H <= 8192 && I <= 8192 && E <= kMaxPlanExperts &&
-           static_cast<long long>(T) * kMaxTopk < (1LL << 30);
+    // NVFP4 also needs K % 256 == 0 (16-byte loads of 4 slices' scale bytes per row)
+    return T > kMaxRowsPerSweep && H <= 8192 && I <= 8192 && E <= kMaxPlanExperts &&
+           static_cast<long long>(T) * kMaxTopk < (1LL << 30) &&
+           (fmt == 0 || (H % 256 == 0 && I % 256 == 0));
 }
 
 
@@ -234,14 +236,14 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
             size_t ws_bytes, int32_t* err, cudaStream_t s) {
     int rc = check_sizes(T, H, I, E, topk);
     if (rc) return rc;
-    if (FMT == 0 && uses_prefill(T, H, I, E, 0)) {
+    if (uses_prefill(T, H, I, E, FMT)) {
         if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
         const PrefillLayout L = prefill_layout(T, H, I, E, topk);
         if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-        return cuda_status(launch_prefill_fp8(
-            reinterpret_cast<const __nv_bfloat16*>(x), T, H, I, E, topk, ids, wts, pg.w, pg.s, pu.w,
-            pu.s, pd.w, pd.s, limit, reinterpret_cast<__nv_bfloat16*>(out),
-            static_cast<uint8_t*>(ws), L, err, s));
+        PrefillWeights wt{pg.w, pu.w, pd.w, pg.s, pu.s, pd.s, pg.sf, pu.sf, pd.sf, pg.s2, pu.s2, pd.s2};
+        return cuda_status(launch_prefill(FMT, reinterpret_cast<const __nv_bfloat16*>(x), T, H, I, E, topk,
+                                          ids, wts, wt, limit, reinterpret_cast<__nv_bfloat16*>(out),
+                                          static_cast<uint8_t*>(ws), L, err, s));
     }
     const int rows_max = rows_per_sweep(T);
     Ws w;

@@ -57,12 +57,18 @@ struct PrefillLayout {
     size_t x16, xinv, amax, a16, ainv, f32, total;
 };
 PrefillLayout prefill_layout(int T, int H, int I, int E, int topk);
-cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
-                               const int32_t* ids, const float* wts, const uint8_t* wg,
-                               const float* sg, const uint8_t* wu, const float* su,
-                               const uint8_t* wd, const float* sd, float limit,
-                               __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L,
-                               int32_t* err, cudaStream_t stream);
+// Weights of the three projections for the prefill tier: FP8 codes + fp32 block scales, or
+// NVFP4 packed codes + E4M3 scale bytes + scale_2.
+struct PrefillWeights {
+    const uint8_t *wg, *wu, *wd;
+    const float *sg, *su, *sd;        // FP8
+    const uint8_t *sfg, *sfu, *sfd;   // NVFP4
+    float s2g, s2u, s2d;              // NVFP4
+};
+cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
+                           const int32_t* ids, const float* wts, const PrefillWeights& wt, float limit,
+                           __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L, int32_t* err,
+                           cudaStream_t stream);
 
 // Route histogram / stable counting sort, optionally emitting expert groups (route_plan.cu).
 cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,

@@ -421,12 +421,13 @@ int gemm_grid() {
 
 }  // namespace
 
-cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
-                               const int32_t* ids, const float* wts, const uint8_t* wg,
-                               const float* sg, const uint8_t* wu, const float* su,
-                               const uint8_t* wd, const float* sd, float limit,
-                               __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L,
-                               int32_t* err, cudaStream_t stream) {
+cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
+                           const int32_t* ids, const float* wts, const PrefillWeights& wt, float limit,
+                           __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L, int32_t* err,
+                           cudaStream_t stream) {
+    if (fmt == 1 && MOE_PREFILL_TC != 4) return cudaErrorNotSupported;   // NVFP4: TMEM core only
+    const uint8_t *wg = wt.wg, *wu = wt.wu, *wd = wt.wd;
+    const float *sg = wt.sg, *su = wt.su, *sd = wt.sd;
     const int P = T * topk;
     auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
     cudaError_t st;
@@ -480,6 +481,11 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     gu.err = err;
     gu.a_rows = MOE_PREFILL_TC >= 3 ? P : T;
     gu.experts = E;
+    gu.fmt = fmt;
+    gu.sf0 = wt.sfg;
+    gu.sf1 = wt.sfu;
+    gu.s2_0 = wt.s2g;
+    gu.s2_1 = wt.s2u;
     if (MOE_PREFILL_TC == 4) {
         if ((st = launch_prefill_gemm_tw(0, gu, I, stream)) != cudaSuccess) return st;
     } else if (MOE_PREFILL_TC == 3) {
@@ -508,6 +514,10 @@ cudaError_t launch_prefill_fp8(const __nv_bfloat16* x, int T, int H, int I, int 
     dn.w1 = wd;
     dn.s1 = sd;
     dn.wrows = H;
+    dn.sf0 = wt.sfd;
+    dn.sf1 = wt.sfd;
+    dn.s2_0 = wt.s2d;
+    dn.s2_1 = wt.s2d;
     dn.out = f32;
     dn.amax = nullptr;
     dn.out_ld = H;

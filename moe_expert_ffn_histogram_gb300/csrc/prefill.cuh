@@ -47,6 +47,12 @@ struct PrefillGemmArgs {
     int32_t* err;                // optional error word (bit 1: a bounded wait gave up)
     int a_rows;                  // rows of the A matrix: T (KIND 0) or P (KIND 1)
     int experts;                 // E
+    // NVFP4 weights (prefill_tw.cu only): w0/w1 hold packed E2M1 codes [E][wrows][K/2], sf0/sf1
+    // the E4M3 scale bytes [E][wrows][K/16], s2_0/s2_1 the per-projection scale_2
+    int fmt;                     // 0 FP8 E4M3 block-128, 1 NVFP4
+    const uint8_t* sf0;
+    const uint8_t* sf1;
+    float s2_0, s2_1;
 };
 
 // (m-tile, n-tile) of work item `tile` in expert-major, n-tile-middle, m-tile-minor order: the
@@ -86,7 +92,8 @@ cudaError_t launch_prefill_gemm_ws(int kind, const PrefillGemmArgs& p, int N_tot
 // TMA-fed variant of the warp-specialised core (prefill_tma.cu): A and the E4M3 weight slices
 // arrive by tensor-map copies (a row gather for the gate/up activations).
 cudaError_t launch_prefill_gemm_tma(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
-// Transposed variant with the dequantised weights as the MMA's TMEM operand (prefill_tw.cu).
+// Transposed variant with the dequantised weights as the MMA's TMEM operand (prefill_tw.cu);
+// FP8 or NVFP4 weights (p.fmt).
 cudaError_t launch_prefill_gemm_tw(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
 
 }  // namespace moe

@@ -48,10 +48,13 @@ constexpr int kTwEpiWarps = 8;
 constexpr int kTwMmaWarp = kTwEpiWarp0 + kTwEpiWarps;      // 20
 constexpr int kTwThreads = 32 * (kTwMmaWarp + 1);          // 672
 
-template <int NM, int DB>
+template <int NM, int DB, int FMT>
 struct TwCfg {
-    static constexpr int kRaw = NM * 128 * 64;             // raw E4M3 boxes of one slice
-    static constexpr int kSmem = kTwSlots * kTwTok + kTwRawStages * kRaw + 1024;
+    static constexpr int kRowBytes = FMT == 0 ? 64 : 32;   // raw bytes of one row's 64-wide slice
+    static constexpr int kRaw = NM * 128 * kRowBytes;      // raw weight boxes of one slice
+    // (at least 120 KB, so that one CTA - and one 512-column TMEM allocation - fits per SM)
+    static constexpr int kSmemUsed = kTwSlots * kTwTok + kTwRawStages * kRaw + 1024;
+    static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
     static constexpr int kAcc = DB ? 2 : 1;                // accumulator buffers
     static constexpr uint32_t kAccCols = NM * 128;         // one buffer: NM matrices x 128 tokens
     static constexpr uint32_t kACols = NM * 32;            // one slot: 64 K (32 f16 pairs) per matrix
@@ -63,11 +66,11 @@ struct TwCfg {
 
 }  // namespace
 
-template <int KIND, int NM, int DB>
+template <int KIND, int NM, int DB, int FMT>
 __global__ void __launch_bounds__(kTwThreads, 1)
     prefill_tw_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ CUtensorMap tmTok,
                            const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1) {
-    using Cfg = TwCfg<NM, DB>;
+    using Cfg = TwCfg<NM, DB, FMT>;
     constexpr int NS = kTwSlots, NR = kTwRawStages;
     constexpr uint32_t kIdesc128 = idesc_f16_f32<128, 128>();
     extern __shared__ uint8_t smem_dyn[];
@@ -145,8 +148,10 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&rfull[r], Cfg::kRaw);
-                        tma_load_2d(smem_u32(stRaw(r)), &tmW0, kt * 64, wy, &rfull[r]);
-                        if (NM == 2) tma_load_2d(smem_u32(stRaw(r)) + 128 * 64, &tmW1, kt * 64, wy, &rfull[r]);
+                        tma_load_2d(smem_u32(stRaw(r)), &tmW0, kt * Cfg::kRowBytes, wy, &rfull[r]);
+                        if (NM == 2)
+                            tma_load_2d(smem_u32(stRaw(r)) + 128 * Cfg::kRowBytes, &tmW1, kt * Cfg::kRowBytes, wy,
+                                        &rfull[r]);
                     }
                 }
                 if (!ok) {
@@ -163,28 +168,38 @@ __global__ void __launch_bounds__(kTwThreads, 1)
         // released as soon as it is in registers; the TMEM slot is waited for only then.
         const int cw = warp - kTwConvWarp0, qd = warp & 3, part = cw / 4;
         const int rrow = (NM == 2 ? part * 128 : 0) + 32 * qd + lane;       // raw row of this thread
-        constexpr int kChunks = NM == 2 ? 4 : 2;                             // 16-byte chunks per slice
-        const int c0 = NM == 2 ? 0 : 2 * part;
-        const int sw = (rrow >> 1) & 3;
         const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+        // FP8: 16-byte chunks of 16 codes, 64-byte rows, 64-byte swizzle. NVFP4: 16-byte chunks of
+        // 32 codes, 32-byte rows, 32-byte swizzle (chunk ^ bit 2 of the row).
+        constexpr int kChunks = FMT == 0 ? (NM == 2 ? 4 : 2) : (NM == 2 ? 2 : 1);
+        const int c0 = NM == 2 ? 0 : kChunks * part;
+        const int sw = FMT == 0 ? (rrow >> 1) & 3 : (rrow >> 2) & 1;
         uint32_t* tbl = w_scale[cw];
+        const uint8_t* sfrow = nullptr;                    // NVFP4: this row's scale bytes
+        uint4 sfv = make_uint4(0, 0, 0, 0);                // NVFP4: scale bytes of 4 slices (K 256)
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
             int mt, nt;
             decode_tile(p, tile, mt, nt);
             const int e = p.tile_e[mt];
-            __syncwarp();                                  // the old table is no longer read
-            const size_t sblk = static_cast<size_t>(e) * (p.wrows / 128) + nt;
-            weight_prescale((NM == 2 && part == 1 ? p.s1 : p.s0) + sblk * KB, KB, tbl);
-            __syncwarp();
+            if constexpr (FMT == 0) {
+                __syncwarp();                              // the old table is no longer read
+                const size_t sblk = static_cast<size_t>(e) * (p.wrows / 128) + nt;
+                weight_prescale((NM == 2 && part == 1 ? p.s1 : p.s0) + sblk * KB, KB, tbl);
+                __syncwarp();
+            } else {
+                const size_t wr_ = static_cast<size_t>(e) * p.wrows + nt * 128 + (rrow & 127);
+                sfrow = (NM == 2 && part == 1 ? p.sf1 : p.sf0) + wr_ * (K / 16);
+            }
             bool ok = true;
             for (int kt = 0; kt < KT; ++kt, ++sc) {
                 const uint32_t r = sc % NR, ur = sc / NR, s = sc % NS, us = sc / NS;
+                if (FMT == 1 && (kt & 3) == 0) sfv = __ldg(reinterpret_cast<const uint4*>(sfrow + kt * 4));
                 if (!__all_sync(0xffffffffu, mbar_wait(&rfull[r], ur & 1u))) {
                     ok = false;
                     break;
                 }
-                const uint8_t* raw = stRaw(r) + rrow * 64;
+                const uint8_t* raw = stRaw(r) + rrow * Cfg::kRowBytes;
                 uint4 wr[kChunks];
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) wr[c] = lds128(raw + (((c0 + c) ^ sw) << 4));
@@ -194,17 +209,35 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t sc2 = tbl[kt >> 1];
-                uint32_t h[8 * kChunks];
+                uint32_t h[NM == 2 ? 32 : 16];
+                if constexpr (FMT == 0) {
+                    const uint32_t sc2 = tbl[kt >> 1];
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    const uint32_t wv[4] = {wr[c].x, wr[c].y, wr[c].z, wr[c].w};
+                    for (int c = 0; c < kChunks; ++c) {
+                        const uint32_t wv[4] = {wr[c].x, wr[c].y, wr[c].z, wr[c].w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t lo, hi;
-                        e4m3x4_to_f16x2x2(wv[i], lo, hi);
-                        h[8 * c + 2 * i] = hmul2(lo, sc2);
-                        h[8 * c + 2 * i + 1] = hmul2(hi, sc2);
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t lo, hi;
+                            e4m3x4_to_f16x2x2(wv[i], lo, hi);
+                            h[8 * c + 2 * i] = hmul2(lo, sc2);
+                            h[8 * c + 2 * i + 1] = hmul2(hi, sc2);
+                        }
+                    }
+                } else {
+                    // the slice's 4 scale bytes (one per 16 codes); E2M1 x E4M3 products are exact
+                    const uint32_t sfw = (kt & 2) ? ((kt & 1) ? sfv.w : sfv.z) : ((kt & 1) ? sfv.y : sfv.x);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        const uint32_t wv[4] = {wr[c].x, wr[c].y, wr[c].z, wr[c].w};
+                        const int grp0 = 2 * (c0 + c);     // scale group of the chunk's first 16 codes
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t sf2 = e4m3_splat_f16x2((sfw >> (8 * (grp0 + (i >> 1)))) & 0xFFu);
+                            uint32_t q[4];
+                            e2m1x8_to_f16x2x4(wv[i], q[0], q[1], q[2], q[3]);
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) h[16 * c + 4 * i + b] = hmul2(q[b], sf2);
+                        }
                     }
                 }
                 const uint32_t ta = tmem + lane_off + Cfg::kA0 + s * Cfg::kACols + (NM == 2 ? part * 32 : part * 16);
@@ -283,8 +316,14 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 xs_s[ew][32 * i + lane] = KIND == 0 ? p.a_inv[p.sorted_pair[rr] / p.topk] : p.a_inv[rr];
             }
             const size_t sblk = static_cast<size_t>(e) * (p.wrows / 128) + nt;
-            const float winv0 = weight_prescale(p.s0 + sblk * KB, KB, nullptr);
-            const float winv1 = KIND == 0 ? weight_prescale(p.s1 + sblk * KB, KB, nullptr) : winv0;
+            float winv0, winv1;                            // undo the converters' weight scaling
+            if constexpr (FMT == 0) {
+                winv0 = weight_prescale(p.s0 + sblk * KB, KB, nullptr);
+                winv1 = KIND == 0 ? weight_prescale(p.s1 + sblk * KB, KB, nullptr) : winv0;
+            } else {
+                winv0 = p.s2_0;                            // NVFP4: scale_2 of the projection
+                winv1 = KIND == 0 ? p.s2_1 : winv0;
+            }
             __syncwarp();
             const uint32_t b = tcount % Cfg::kAcc, v = tcount / Cfg::kAcc;
             if (!__all_sync(0xffffffffu, mbar_wait_sleep(&acc_full[b], v & 1u))) {
@@ -359,26 +398,27 @@ PFN_cuTensorMapEncodeTiled_v12000 tw_encoder() {
     return fn;
 }
 
-// 2-D map over a row-major [rows][inner] matrix of elem-byte elements, box 64 x 128.
+// 2-D map over a row-major [rows][inner] matrix of elem-byte elements, box box_inner x 128.
 bool tw_map(CUtensorMap* m, CUtensorMapDataType dt, int elem, const void* base, uint64_t inner, uint64_t rows,
-            CUtensorMapSwizzle sw) {
+            uint32_t box_inner, CUtensorMapSwizzle sw) {
     auto enc = tw_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {inner, rows};
     const cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem)};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {box_inner, 128};
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KIND, int NM, int DB>
+template <int KIND, int NM, int DB, int FMT>
 cudaError_t launch_tw(const PrefillGemmArgs& q, const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
                       int grid, cudaStream_t stream) {
-    cudaError_t st = cudaFuncSetAttribute(prefill_tw_gemm_kernel<KIND, NM, DB>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, TwCfg<NM, DB>::kSmem);
+    using Cfg = TwCfg<NM, DB, FMT>;
+    cudaError_t st = cudaFuncSetAttribute(prefill_tw_gemm_kernel<KIND, NM, DB, FMT>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (st != cudaSuccess) return st;
-    prefill_tw_gemm_kernel<KIND, NM, DB><<<grid, kTwThreads, TwCfg<NM, DB>::kSmem, stream>>>(q, a, w0, w1);
+    prefill_tw_gemm_kernel<KIND, NM, DB, FMT><<<grid, kTwThreads, Cfg::kSmem, stream>>>(q, a, w0, w1);
     return cudaGetLastError();
 }
 
@@ -397,12 +437,21 @@ cudaError_t launch_prefill_gemm_tw(int kind, const PrefillGemmArgs& p, int N_tot
     q.n_tiles = N_total / 128;
     CUtensorMap ma, mw0, mw1;
     const uint64_t wrows_all = static_cast<uint64_t>(p.experts) * p.wrows;
-    const bool ok = tw_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.a, p.K, p.a_rows, CU_TENSOR_MAP_SWIZZLE_128B) &&
-                    tw_map(&mw0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w0, p.K, wrows_all, CU_TENSOR_MAP_SWIZZLE_64B) &&
-                    tw_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w1, p.K, wrows_all, CU_TENSOR_MAP_SWIZZLE_64B);
+    const bool fp4 = p.fmt == 1;
+    if (fp4 && ((reinterpret_cast<uintptr_t>(p.sf0) | reinterpret_cast<uintptr_t>(p.sf1)) & 15u))
+        return cudaErrorMisalignedAddress;
+    // FP8: rows of K code bytes, boxes of 64 bytes (64-byte swizzle); NVFP4: rows of K/2 bytes of
+    // packed codes, boxes of 32 bytes (32-byte swizzle)
+    const uint64_t wbytes = fp4 ? p.K / 2 : p.K;
+    const uint32_t wbox = fp4 ? 32 : 64;
+    const CUtensorMapSwizzle wsw = fp4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const bool ok = tw_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.a, p.K, p.a_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                    tw_map(&mw0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w0, wbytes, wrows_all, wbox, wsw) &&
+                    tw_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w1, wbytes, wrows_all, wbox, wsw);
     if (!ok) return cudaErrorInvalidValue;
-    if (kind == 0) return launch_tw<0, 2, 0>(q, ma, mw0, mw1, sms, stream);
-    return launch_tw<1, 1, 1>(q, ma, mw0, mw1, sms, stream);
+    if (kind == 0) return fp4 ? launch_tw<0, 2, 0, 1>(q, ma, mw0, mw1, sms, stream)
+                              : launch_tw<0, 2, 0, 0>(q, ma, mw0, mw1, sms, stream);
+    return fp4 ? launch_tw<1, 1, 1, 1>(q, ma, mw0, mw1, sms, stream) : launch_tw<1, 1, 1, 0>(q, ma, mw0, mw1, sms, stream);
 }
 
 }  // namespace moe

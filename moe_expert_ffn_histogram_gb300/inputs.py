@@ -16,6 +16,8 @@ stand in for them, with the pages' shapes):
   overlap across tokens.
 * ``nvfp4_decode`` - T=1, H=5120, I=1536, E=160, NVFP4 W4A16.
 * ``fp8_prefill`` - T=4096 over the fp8_decode bank; routes from a Zipf(1.1) expert popularity.
+* ``nvfp4_prefill`` - T=4096 over the nvfp4_decode bank; Zipf(1.1) routes (the second prefill
+  workload: the grouped GEMM over W4A16 banks).
 
 All weights are N(0, 0.02) in fp32 before quantisation; router weights are a softmax of N(0, 1)
 logits over the 8 slots; activations are N(0, 1) bf16 (LCG for the tiny case); limit = 7.
@@ -48,6 +50,8 @@ CONFIGS = {
                          seed=1004, bank_seed=1004),
     "fp8_prefill": dict(fmt="fp8", T=4096, H=7168, I=2048, E=256, routes="zipf", x="normal",
                         seed=1005, bank_seed=1002),
+    "nvfp4_prefill": dict(fmt="nvfp4", T=4096, H=5120, I=1536, E=160, routes="zipf", x="normal",
+                          seed=1006, bank_seed=1004),
 }
 LIMIT = 7.0
 

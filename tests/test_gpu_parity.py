@@ -278,6 +278,40 @@ def test_prefill_clamp_stress_and_no_limit():
     check_close(bf16_to_f64(run(wl2)), oracle_for(wl2)["out"], "prefill no limit")
 
 
+# ---- the grouped-GEMM tier over NVFP4 banks (K multiples of 256) -------------------------------------
+
+@pytest.mark.parametrize("T,H,I,E,routes", [(9, 256, 256, 16, "uniform"), (64, 512, 256, 40, "zipf"),
+                                            (300, 256, 512, 8, "uniform"), (130, 768, 512, 24, "zipf")])
+def test_nvfp4_prefill_parity(T, H, I, E, routes):
+    wl = inputs.make_custom("nvfp4", T, H, I, E, seed=900 + T, device=DEV, routes=routes)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"nvfp4 prefill T={T} E={E}")
+
+
+def test_nvfp4_prefill_skewed_bad_ids_and_clamp():
+    T, E = 200, 12
+    wl = inputs.make_custom("nvfp4", T, 512, 256, E, seed=901, device=DEV, x_scale=30.0)
+    ids = wl.ids.clone()
+    ids[:150, :4] = torch.tensor([0, 1, 2, 3], dtype=torch.int32, device=DEV)
+    ids[5, 6] = -1
+    ids[7, 2] = E + 3
+    wl.ids = ids
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(wl, err=err)
+    assert int(err.item()) & capi.ERRBIT_BAD_ID
+    check_close(bf16_to_f64(out), oracle_for(wl)["out"], "nvfp4 prefill skew")
+    a = out.clone()
+    assert torch.equal(run(wl, err=err).view(torch.int16), a.view(torch.int16))
+
+
+def test_nvfp4_prefill_full_size_sampled():
+    bank = inputs.make_bank("nvfp4_prefill", DEV)
+    wl = inputs.make_workload("nvfp4_prefill", device=DEV, bank=bank)
+    out = run(wl)
+    toks = [0, 5, 1000, 2047, 4095]
+    res = oracle_for(wl, tokens=toks)
+    check_close(bf16_to_f64(out[toks]), res["out"], "nvfp4_prefill sampled")
+
+
 def test_prefill_bitwise_repeatable():
     wl = inputs.make_custom("fp8", 100, 256, 256, 16, seed=804, device=DEV, routes="zipf")
     a = run(wl).clone()

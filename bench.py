@@ -324,6 +324,24 @@ def bench_ours(args):
             stage_ms["down_combine"].append(e2.elapsed_time(e3))
     clk = clocks.stop()
 
+    # ---- the router in front of the path (informational): a synthetic bf16 router matrix
+    rg = torch.Generator(device=dev)
+    rg.manual_seed(4242)
+    rw = (torch.randn(E, wl0.H, generator=rg, device=dev) * wl0.H ** -0.5).to(torch.bfloat16)
+    rbias = torch.zeros(E, dtype=torch.float32, device=dev)
+    router_ms = []
+    if E % 16 == 0 and E <= 1024:
+        rws = torch.empty(int(capi.load().moe_router_workspace_bytes(T, wl0.H, E)), dtype=torch.uint8, device=dev)
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            capi.router(sets[i % N_ROUTE_SETS].x, rw, 8, 2.5, True, bias=rbias, workspace=rws)
+            b_.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                router_ms.append(a_.elapsed_time(b_))
+
     # ---- end to end through the public API: pinned host inputs in, result out, every step
     hx = [s.x.cpu().pin_memory() for s in sets]
     hids = [s.ids.cpu().pin_memory() for s in sets]
@@ -419,6 +437,10 @@ def bench_ours(args):
         "stage_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in stage_ms.items() if v},
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,
+        "router": None if not router_ms else {
+            "us": round(statistics.mean(router_ms) * 1e3, 2), "T": T, "E": E, "H": wl0.H,
+            "weight_gbs": round(E * wl0.H * 2 / (statistics.mean(router_ms) * 1e-3) / 1e9, 1),
+            "note": "moe_router (logits GEMV/GEMM + top-8), not part of the step"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 5)},
         "clocks": clk,

@@ -218,6 +218,33 @@ MOE_API int moe_fp8_forward_noalloc(const uint16_t* x, int T, int H, int I, int 
                                     const uint8_t* w_down, const float* s_down, float limit,
                                     uint16_t* out, int32_t* err, void* stream);
 
+/*
+ * moe_router - the router in front of the FFN: logits, sigmoid, selection bias, top-k, weights.
+ * ("spark_model layers/glm5next_mlp/forward.rs", `forward_moe` router step: one f32-output logits
+ * GEMM over all rows, then one top-k launch taking logits, router_bias, top_k, n_group = 1,
+ * routed_scale, renormalize; the Step gate's sigmoid top-k router takes the same router matrix,
+ * bias, top_k, router_scale and route_norm.)
+ *
+ *   x            [T][H]  bf16 (device).         router_w [E][H] bf16 (device, K = H contiguous).
+ *   bias         [E] fp32 selection bias (device) or NULL for none.
+ *   logits       [T][E] fp32 out (device) or NULL: l = sum_h x[t][h] * router_w[e][h], fp32 MMA
+ *                accumulation.
+ *   topk_ids     [T][topk] int32 out: experts by descending sigmoid(l) + bias; equal scores go to
+ *                the lower expert index (the pages print no tie rule; this is the stable one).
+ *   topk_weights [T][topk] fp32 out: sigmoid(l) of each pick (the bias only selects), divided by
+ *                the sum over the picks if renormalize != 0, times routed_scale.
+ *   workspace    >= moe_router_workspace_bytes(T, H, E) bytes (device, 256-byte aligned): partial
+ *                logits of a K split for small T.
+ * Limits: 16 <= E <= 1024 with E % 16 == 0, H % 32 == 0, 1 <= topk <= min(8, E), routed_scale
+ * finite and > 0, x and router_w 16-byte aligned. Errors return synchronously (MOE_ERR_*) with
+ * nothing enqueued; otherwise two launches on `stream`, no host synchronisation. Deterministic.
+ */
+MOE_API size_t moe_router_workspace_bytes(int T, int H, int E);
+MOE_API int moe_router(const uint16_t* x, int T, int H, const uint16_t* router_w, const float* bias,
+                       int E, int topk, float routed_scale, int renormalize, float* logits,
+                       int32_t* topk_ids, float* topk_weights, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* Library build identification: the compiled CUDA architecture string (e.g. "sm_103a"). */
 MOE_API const char* moe_build_arch(void);
 

@@ -24,7 +24,8 @@ ERRBIT_BAD_ID = 1
 
 EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_nvfp4_forward",
             "moe_plan", "moe_fp8_gate_up", "moe_fp8_down_combine", "moe_nvfp4_gate_up",
-            "moe_nvfp4_down_combine", "moe_build_arch", "moe_fp8_forward_noalloc")
+            "moe_nvfp4_down_combine", "moe_build_arch", "moe_fp8_forward_noalloc",
+            "moe_router_workspace_bytes", "moe_router")
 
 _lib = None
 
@@ -75,6 +76,10 @@ def load(path: Optional[str] = None):
                                            sz, vp]
     lib.moe_build_arch.restype = ctypes.c_char_p
     lib.moe_build_arch.argtypes = []
+    lib.moe_router_workspace_bytes.restype = sz
+    lib.moe_router_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.moe_router.restype = i32
+    lib.moe_router.argtypes = [vp, i32, i32, vp, vp, i32, i32, f32, i32, vp, vp, vp, vp, sz, vp]
     if path is None:
         _lib = lib
     return lib
@@ -249,3 +254,30 @@ def down_combine(ids, wts, bank, out, workspace, stream=None):
 
 def build_arch() -> str:
     return load().moe_build_arch().decode()
+
+
+def router(x: torch.Tensor, router_w: torch.Tensor, topk: int, routed_scale: float = 1.0,
+           renormalize: bool = True, bias: Optional[torch.Tensor] = None, want_logits: bool = False,
+           workspace: Optional[torch.Tensor] = None, stream=None):
+    """moe_router: (topk_ids [T,topk] int32, topk_weights [T,topk] fp32, logits [T,E] fp32 or None)."""
+    dev = x.device
+    _need(x, "x", torch.bfloat16, dev)
+    _need(router_w, "router_w", torch.bfloat16, dev)
+    T, H = x.shape
+    E = router_w.shape[0]
+    if bias is not None:
+        _need(bias, "bias", torch.float32, dev)
+    lib = load()
+    if workspace is None:
+        n = int(lib.moe_router_workspace_bytes(T, H, E))
+        if n == 0:
+            raise ValueError("invalid sizes for moe_router_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    ids = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None
+    rc = lib.moe_router(_ptr(x), T, H, _ptr(router_w), _ptr(bias), E, topk, float(routed_scale),
+                        int(bool(renormalize)), _ptr(logits), _ptr(ids), _ptr(wts), _ptr(workspace),
+                        workspace.numel(), _stream(dev, stream))
+    _check("moe_router", rc)
+    return ids, wts, logits

@@ -423,6 +423,48 @@ int moe_nvfp4_down_combine(int T, int H, int I, int E, int topk, const int32_t* 
                          scale2_down, out, w, static_cast<cudaStream_t>(stream));
 }
 
+// ---- router ---------------------------------------------------------------------------------
+
+namespace {
+bool router_shape_ok(int T, int H, int E) {
+    return T >= 1 && H >= 32 && H % 32 == 0 && E >= 16 && E <= 1024 && E % 16 == 0;
+}
+int device_sms(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+}  // namespace
+
+size_t moe_router_workspace_bytes(int T, int H, int E) {
+    if (!router_shape_ok(T, H, E)) return 0;
+    int sms = 0;
+    if (device_sms(&sms) != MOE_OK) sms = 152;
+    const int ks = router_ksplit(T, H, E, sms);
+    return align_up(static_cast<size_t>(ks) * T * E * sizeof(float), 256);
+}
+
+int moe_router(const uint16_t* x, int T, int H, const uint16_t* router_w, const float* bias, int E, int topk,
+               float routed_scale, int renormalize, float* logits, int32_t* topk_ids, float* topk_weights,
+               void* workspace, size_t workspace_bytes, void* stream) {
+    if (!x || !router_w || !topk_ids || !topk_weights) return MOE_ERR_NULL;
+    if (!router_shape_ok(T, H, E) || topk < 1 || topk > kMaxTopk || topk > E) return MOE_ERR_SHAPE;
+    if (!std::isfinite(routed_scale) || !(routed_scale > 0.0f)) return MOE_ERR_VALUE;
+    if (!all_aligned(x, router_w)) return MOE_ERR_ALIGN;
+    if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MOE_ERR_WORKSPACE;
+    int sms = 0;
+    int rc = device_sms(&sms);
+    if (rc) return rc;
+    const int ks = router_ksplit(T, H, E, sms);
+    if (workspace_bytes < static_cast<size_t>(ks) * T * E * sizeof(float)) return MOE_ERR_WORKSPACE;
+    if (router_topk_smem_bytes(E) > kMaxSmem) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_router(reinterpret_cast<const __nv_bfloat16*>(x), T, H,
+                                     reinterpret_cast<const __nv_bfloat16*>(router_w), bias, E, topk, routed_scale,
+                                     renormalize != 0, logits, topk_ids, topk_weights, static_cast<float*>(workspace),
+                                     ks, static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_build_arch(void) { return "sm_103a"; }
 
 }  // extern "C"

@@ -70,6 +70,13 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
                            __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L, int32_t* err,
                            cudaStream_t stream);
 
+// Router (router.cu): K-split factor for (T, H, E), top-k shared memory, and the two launches.
+int router_ksplit(int T, int H, int E, int sms);
+size_t router_topk_smem_bytes(int E);
+cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloat16* w, const float* bias, int E,
+                          int topk, float routed_scale, int renorm, float* logits, int32_t* ids, float* wts,
+                          float* part, int KS, cudaStream_t stream);
+
 // Route histogram / stable counting sort, optionally emitting expert groups (route_plan.cu).
 cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,
                               int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,

@@ -1,0 +1,176 @@
+// Router in front of the routed FFN: fp32 logits = bf16 x . bf16 router rows, then sigmoid, a
+// per-expert selection bias, top-k, optional renormalisation and routed_scale
+// ("spark_model layers/glm5next_mlp/forward.rs", `forward_moe` router step: one logits GEMM with
+// f32 output for all rows, then one top-k launch over all rows taking logits, router_bias, top_k,
+// n_group = 1, routed_scale and renormalize; the Step gate builds the same sigmoid top-k router from
+// its router matrix, bias, top_k, router_scale and route_norm).
+//
+//   router_logits_kernel: tensor-core GEMV/GEMM. A = 16 router rows per warp (bf16 straight from
+//     HBM, no conversion), B = 8 tokens per MMA column tile, mma.sync m16n8k16 bf16 -> f32, with
+//     the lane layout of the FFN kernels (lane c streams 16 bytes of each of its two rows per
+//     32-wide K chunk; elements 4i+{0,1} / 4i+{2,3} are logical K (2c,2c+1) / (2c+8,2c+9) of step
+//     i, and B is read at the same physical positions). Single-token and few-token calls split K
+//     over the grid's z dimension (partial logits in the workspace) so that enough warps stream
+//     the router matrix; wide calls take 32 tokens per CTA so that the matrix is re-read from L2
+//     once per 32 tokens.
+//   router_topk_kernel: one warp per token sums the K parts in order, computes sigmoid and score,
+//     and selects top-k by repeated warp arg-max (score descending, ties to the lower expert
+//     index); weights are the picks' sigmoids (renormalised in pick order, times routed_scale).
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRtWarps = 4;                       // expert tiles of 16 per logits CTA
+constexpr int kRtTopkWarps = 4;                   // tokens per top-k CTA
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// part[ks][t][e] for K chunks (32 wide) [ks*NC/KS, (ks+1)*NC/KS), tokens blockIdx.y*8*TS ..
+template <int TS>
+__global__ void __launch_bounds__(kRtWarps * 32) router_logits_kernel(const __nv_bfloat16* __restrict__ x, int T,
+                                                                     int H, const __nv_bfloat16* __restrict__ w,
+                                                                     int E, float* __restrict__ part) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int e0 = (blockIdx.x * kRtWarps + warp) * 16;
+    if (e0 >= E) return;
+    const int KS = gridDim.z, ks = blockIdx.z, NC = H / 32;
+    const int k0 = ks * NC / KS, k1 = (ks + 1) * NC / KS;
+    const int tbase = blockIdx.y * 8 * TS;
+    const uint4* ra = reinterpret_cast<const uint4*>(w + static_cast<size_t>(e0 + g) * H + c * 8);
+    const uint4* rb = reinterpret_cast<const uint4*>(w + static_cast<size_t>(e0 + g + 8) * H + c * 8);
+    const uint4* xb[TS];
+    bool tv[TS];
+#pragma unroll
+    for (int j = 0; j < TS; ++j) {
+        const int t = tbase + 8 * j + g;
+        tv[j] = t < T;
+        xb[j] = reinterpret_cast<const uint4*>(x + static_cast<size_t>(tv[j] ? t : 0) * H + c * 8);
+    }
+    float acc[TS][4];
+#pragma unroll
+    for (int j = 0; j < TS; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    for (int kc = k0; kc < k1; ++kc) {
+        const uint4 qa = ld_stream_v4(ra + kc * 4), qb = ld_stream_v4(rb + kc * 4);   // 32 bf16 = 4 uint4
+#pragma unroll
+        for (int j = 0; j < TS; ++j) {
+            const uint4 bx = tv[j] ? __ldg(xb[j] + kc * 4) : make_uint4(0, 0, 0, 0);
+            mma_bf16(acc[j], qa.x, qb.x, qa.y, qb.y, bx.x, bx.y);
+            mma_bf16(acc[j], qa.z, qb.z, qa.w, qb.w, bx.z, bx.w);
+        }
+    }
+    float* dst = part + static_cast<size_t>(ks) * T * E;
+#pragma unroll
+    for (int j = 0; j < TS; ++j) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int t = tbase + 8 * j + 2 * c + (q & 1), e = e0 + g + 8 * (q >> 1);
+            if (t < T) dst[static_cast<size_t>(t) * E + e] = acc[j][q];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const float* __restrict__ part, int KS,
+                                                                        int T, int E, const float* __restrict__ bias,
+                                                                        int topk, float routed_scale, int renorm,
+                                                                        float* __restrict__ logits,
+                                                                        int32_t* __restrict__ ids,
+                                                                        float* __restrict__ wts) {
+    extern __shared__ float rt_smem[];                // [warps][2][E]: sigmoid, score
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRtTopkWarps + warp;
+    if (t >= T) return;
+    float* sig = rt_smem + static_cast<size_t>(warp) * 2 * E;
+    float* score = sig + E;
+    for (int e = lane; e < E; e += 32) {
+        float l = 0.0f;
+        for (int q = 0; q < KS; ++q) l += part[(static_cast<size_t>(q) * T + t) * E + e];
+        if (logits != nullptr) logits[static_cast<size_t>(t) * E + e] = l;
+        const float s = 1.0f / (1.0f + expf(-l));
+        sig[e] = s;
+        score[e] = s + (bias != nullptr ? bias[e] : 0.0f);
+    }
+    __syncwarp();
+    float picked[kMaxTopk];
+    int pid[kMaxTopk];
+    for (int k = 0; k < topk; ++k) {
+        float bs = -INFINITY;
+        int be = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            const float v = score[e];
+            if (v > bs) {                             // strided scan: first (lowest) index wins ties
+                bs = v;
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (os > bs || (os == bs && oe < be)) {
+                bs = os;
+                be = oe;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) score[be] = -INFINITY;         // taken
+        __syncwarp();
+        pid[k] = be;
+        picked[k] = sig[be];
+    }
+    if (lane == 0) {
+        float sum = 0.0f;
+        for (int k = 0; k < topk; ++k) sum += picked[k];
+        for (int k = 0; k < topk; ++k) {
+            const float wv = renorm ? picked[k] / sum : picked[k];
+            ids[static_cast<size_t>(t) * topk + k] = pid[k];
+            wts[static_cast<size_t>(t) * topk + k] = wv * routed_scale;
+        }
+    }
+}
+
+}  // namespace
+
+int router_ksplit(int T, int H, int E, int sms) {
+    if (T > 32) return 1;
+    const int ctas = ((E / 16 + kRtWarps - 1) / kRtWarps) * ((T + 7) / 8);
+    int ks = (2 * sms + ctas - 1) / ctas;
+    const int nc = H / 32;
+    if (ks > nc / 2) ks = nc / 2;
+    if (ks > 64) ks = 64;
+    return ks < 1 ? 1 : ks;
+}
+
+size_t router_topk_smem_bytes(int E) { return static_cast<size_t>(kRtTopkWarps) * 2 * E * sizeof(float); }
+
+cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloat16* w, const float* bias, int E,
+                          int topk, float routed_scale, int renorm, float* logits, int32_t* ids, float* wts,
+                          float* part, int KS, cudaStream_t stream) {
+    const int ex = (E / 16 + kRtWarps - 1) / kRtWarps;
+    if (T > 32) {
+        router_logits_kernel<4><<<dim3(ex, (T + 31) / 32, KS), kRtWarps * 32, 0, stream>>>(x, T, H, w, E, part);
+    } else {
+        router_logits_kernel<1><<<dim3(ex, (T + 7) / 8, KS), kRtWarps * 32, 0, stream>>>(x, T, H, w, E, part);
+    }
+    cudaError_t st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+    const size_t smem = router_topk_smem_bytes(E);
+    if (smem > 48 * 1024 &&
+        (st = cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(smem))) != cudaSuccess)
+        return st;
+    router_topk_kernel<<<(T + kRtTopkWarps - 1) / kRtTopkWarps, kRtTopkWarps * 32, smem, stream>>>(
+        part, KS, T, E, bias, topk, routed_scale, renorm, logits, ids, wts);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

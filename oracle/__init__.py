@@ -58,7 +58,8 @@ def _load():
         lib.oracle_clamped_swiglu.argtypes = [ctypes.c_double] * 3
         lib.oracle_hardware_threads.restype = ctypes.c_int
         for name in ("oracle_combine", "oracle_dequant_fp8", "oracle_dequant_nvfp4",
-                     "oracle_route_permute", "oracle_moe_fp8", "oracle_moe_nvfp4"):
+                     "oracle_route_permute", "oracle_moe_fp8", "oracle_moe_nvfp4",
+                     "oracle_router_logits", "oracle_router_topk"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -214,3 +215,30 @@ def moe_fp8(x_bf16_bits, ids, wts, bank, limit, tokens=None, intermediates=False
 def moe_nvfp4(x_bf16_bits, ids, wts, bank, limit, tokens=None, intermediates=False, nthreads=0):
     """NVFP4 routed FFN. bank: w_* packed [E,N,K/2] u8, sf_* [E,N,K/16] u8, scale2_* floats."""
     return _forward("nvfp4", x_bf16_bits, ids, wts, bank, limit, tokens, intermediates, nthreads)
+
+
+# ---- router (in front of the FFN) -----------------------------------------------------------------
+
+def router_logits(x_bf16_bits: np.ndarray, w_bf16_bits: np.ndarray) -> np.ndarray:
+    """FP64 logits [T][E] of bf16 x [T][H] against bf16 router rows [E][H]."""
+    x = _c(x_bf16_bits, np.uint16)
+    w = _c(w_bf16_bits, np.uint16)
+    T, H = x.shape
+    E = w.shape[0]
+    out = np.zeros((T, E), dtype=np.float64)
+    rc = _load().oracle_router_logits(_ptr(x), T, H, _ptr(w), E, _ptr(out))
+    assert rc == 0, rc
+    return out
+
+
+def router_topk(logits: np.ndarray, bias, topk: int, routed_scale: float, renormalize: bool):
+    """(ids [T][topk] int32, weights [T][topk] float64) from logits [T][E] (see moe_oracle.cpp)."""
+    lg = _c(logits, np.float64)
+    T, E = lg.shape
+    b = None if bias is None else _c(bias, np.float64)
+    ids = np.zeros((T, topk), dtype=np.int32)
+    wts = np.zeros((T, topk), dtype=np.float64)
+    rc = _load().oracle_router_topk(_ptr(lg), T, E, _ptr(b), topk, ctypes.c_double(routed_scale),
+                                    int(bool(renormalize)), _ptr(ids), _ptr(wts))
+    assert rc == 0, rc
+    return ids, wts

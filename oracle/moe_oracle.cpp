@@ -30,6 +30,16 @@
 // from their bit definitions. Results do not depend on the thread count: each output element is
 // produced by one thread, summing in index order.
 //
+//   * Router (in front of the FFN): fp32 logits = bf16 x . bf16 router rows [E][H]; sigmoid, plus a
+//     per-expert bias for the selection only; top-k by that score; weights = the selected
+//     sigmoids, optionally renormalised to sum 1, times routed_scale; one expert group — "spark_model
+//     layers/glm5next_mlp/forward.rs", `forward_moe` router step (logits GEMM with f32 output, then
+//     one top-k launch taking logits, router_bias, top_k, n_group = 1, routed_scale, renormalize)
+//     and the Step gate's `upload_sigmoid_topk_router(router, bias, top_k, router_scale,
+//     route_norm)`. The pages print no body for the top-k step; the reading here: selection by
+//     sigmoid(l) + bias, descending, ties to the lower expert index; weights from sigmoid(l)
+//     without the bias.
+//
 // Parity pins (tests/test_oracle_pins.py): all 256 E4M3 codes against torch's float8_e4m3fn,
 // the E2M1 magnitude table, hand-built code/scale bytes, clamp boundary values, the pages' combine
 // worked example, brute-force dense float64 matmul on tiny banks, and a brute-force stable sort
@@ -365,6 +375,52 @@ int oracle_moe_nvfp4(const uint16_t* x, int T, int H, int I, int E, int topk, co
     Bank d{2, w_down, nullptr, sf_down, scale2_down, H, I};
     return moe_forward(x, T, H, I, E, topk, ids, wts, g, u, d, limit, token_list, n_tokens,
                        out_f64, out_bf16, g_out, u_out, a_out, y_out, nthreads, err);
+}
+
+// Router logits in double: logits[t][e] = sum_h x[t][h] * W[e][h] (bf16 inputs, exact products).
+int oracle_router_logits(const uint16_t* x, int T, int H, const uint16_t* w, int E, double* logits) {
+    if (T < 1 || H < 1 || E < 1) return -2;
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += bf16_value(x[static_cast<size_t>(t) * H + h]) * bf16_value(w[static_cast<size_t>(e) * H + h]);
+            logits[static_cast<size_t>(t) * E + e] = acc;
+        }
+    return 0;
+}
+
+// Router top-k from given logits, in double: score = sigmoid(l) + bias (bias nullable), the topk
+// largest scores in descending order (ties: lower expert index first); weight = sigmoid(l) of the
+// pick, divided by the sum over the picks when renormalize != 0, times routed_scale.
+int oracle_router_topk(const double* logits, int T, int E, const double* bias, int topk,
+                       double routed_scale, int renormalize, int32_t* ids, double* weights) {
+    if (T < 1 || E < 1 || topk < 1 || topk > E) return -2;
+    std::vector<double> sig(E), score(E);
+    std::vector<char> taken(E);
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            sig[e] = 1.0 / (1.0 + std::exp(-logits[static_cast<size_t>(t) * E + e]));
+            score[e] = sig[e] + (bias ? bias[e] : 0.0);
+            taken[e] = 0;
+        }
+        double sum = 0.0;
+        for (int k = 0; k < topk; ++k) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || score[e] > score[best])) best = e;   // first max wins
+            taken[best] = 1;
+            ids[static_cast<size_t>(t) * topk + k] = best;
+            weights[static_cast<size_t>(t) * topk + k] = sig[best];
+            sum += sig[best];
+        }
+        for (int k = 0; k < topk; ++k) {
+            double& w = weights[static_cast<size_t>(t) * topk + k];
+            if (renormalize) w /= sum;
+            w *= routed_scale;
+        }
+    }
+    return 0;
 }
 
 int oracle_hardware_threads(void) { return resolve_threads(0); }

@@ -132,3 +132,27 @@ def test_stage_entry_points_reject_wide_batches(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         capi.load(str(tmp_path / "missing.so"))
+
+
+def test_router_rejects_bad_arguments(lib):
+    f = lib.moe_router
+
+    def call(**over):
+        a = dict(x=FAKE, T=2, H=256, w=FAKE, bias=None, E=64, topk=8, scale=1.0, renorm=1,
+                 logits=None, ids=FAKE, wts=FAKE, ws=FAKE, ws_bytes=1 << 30, stream=None)
+        a.update(over)
+        return f(*a.values())
+    assert call(x=None) == -1
+    assert call(ids=None) == -1
+    assert call(E=8) == -2                 # fewer than 16 experts
+    assert call(E=100) == -2               # not a multiple of 16
+    assert call(E=2048) == -2
+    assert call(H=250) == -2
+    assert call(topk=9) == -2
+    assert call(topk=0) == -2
+    assert call(scale=0.0) == -4
+    assert call(scale=math.inf) == -4
+    assert call(x=ctypes.c_void_p(0x10000008)) == -7
+    assert call(ws=None) == -3
+    assert lib.moe_router_workspace_bytes(2, 250, 64) == 0
+    assert lib.moe_router_workspace_bytes(2, 256, 64) > 0

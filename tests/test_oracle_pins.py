@@ -301,3 +301,56 @@ def test_oracle_rejects_bad_shapes_and_limit():
         oracle.moe_fp8(wl.x_bits(), wl.ids.numpy(), wl.wts.numpy(), b, limit=0.0)
     with pytest.raises(ValueError):
         oracle.moe_fp8(wl.x_bits(), wl.ids.numpy(), wl.wts.numpy(), b, limit=float("nan"))
+
+
+# ---- router (in front of the FFN) -----------------------------------------------------------------
+
+def test_router_logits_against_numpy_matmul():
+    """FP64 logits of bf16 inputs equal a float64 matmul of the decoded bf16 values."""
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(3, 96, generator=g).to(torch.bfloat16)
+    w = (torch.randn(16, 96, generator=g) * 0.1).to(torch.bfloat16)
+    got = oracle.router_logits(x.view(torch.int16).numpy().view(np.uint16),
+                               w.view(torch.int16).numpy().view(np.uint16))
+    ref = x.to(torch.float64).numpy() @ w.to(torch.float64).numpy().T
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # a transposed operand would change this row: one hot x picks one column of W
+    x1 = torch.zeros(1, 96, dtype=torch.bfloat16)
+    x1[0, 5] = 1.0
+    got1 = oracle.router_logits(x1.view(torch.int16).numpy().view(np.uint16),
+                                w.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(got1[0], w[:, 5].to(torch.float64).numpy())
+
+
+def test_router_topk_closed_forms_ties_and_bias():
+    ln3 = np.log(3.0)
+    # sigmoid(ln 3) = 3/4, sigmoid(0) = 1/2, sigmoid(-ln 3) = 1/4
+    lg = np.array([[0.0, -ln3, ln3, 0.0, -5.0]])
+    ids, w = oracle.router_topk(lg, None, 3, 2.0, True)
+    assert ids.tolist() == [[2, 0, 3]]                      # equal scores: lower index first
+    assert np.allclose(w, [[2.0 * 0.75 / 1.75, 2.0 * 0.5 / 1.75, 2.0 * 0.5 / 1.75]], rtol=1e-14)
+    ids, w = oracle.router_topk(lg, None, 2, 1.5, False)
+    assert ids.tolist() == [[2, 0]] and np.allclose(w, [[1.125, 0.75]], rtol=1e-14)
+    # the bias selects but does not weight: a large bias pulls expert 1 (sigmoid 1/4) to the front
+    bias = np.array([0.0, 10.0, 0.0, 0.0, 0.0])
+    ids, w = oracle.router_topk(lg, bias, 2, 1.0, False)
+    assert ids.tolist() == [[1, 2]] and np.allclose(w, [[0.25, 0.75]], rtol=1e-14)
+
+
+def test_router_topk_against_sort_and_expit():
+    from scipy.special import expit
+    rng = np.random.default_rng(5)
+    T, E, k = 20, 64, 8
+    lg = rng.normal(size=(T, E))
+    lg[3, 10] = lg[3, 40] = lg[3].max() + 1.0               # an exact tie at the top
+    bias = rng.normal(scale=0.1, size=E)
+    bias[40] = bias[10]                                      # ... and equal scores
+    ids, w = oracle.router_topk(lg, bias, k, 2.5, True)
+    sig = expit(lg)
+    score = sig + bias
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -score[t]))[:k]    # descending score, then index
+        assert ids[t].tolist() == order.tolist()
+        sel = sig[t, order]
+        assert np.allclose(w[t], 2.5 * sel / sel.sum(), rtol=1e-12)
+    assert ids[3, 0] == 10 and ids[3, 1] == 40

@@ -129,7 +129,8 @@ template <int FMT>
 int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, const int32_t* ids,
                   const uint8_t* wg, const float* sg, const uint8_t* sfg, float s2g,
                   const uint8_t* wu, const float* su, const uint8_t* sfu, float s2u, float limit,
-                  const Ws& w, int32_t* err, cudaStream_t s) {
+                  const Ws& w, int32_t* err, cudaStream_t s, const uint8_t* wd = nullptr,
+                  const uint8_t* sfd = nullptr) {
     GateUpArgs a{};
     a.x = reinterpret_cast<const __nv_bfloat16*>(x);
     a.H = H;
@@ -149,6 +150,16 @@ int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, co
     a.err = err;
     const int ngroups = rows * topk;     // implicit: topk slots; table: at most one per pair
     const int cap = rows == 1 ? 1 : group_cap(rows, topk);
+    // NVFP4, one token: prefetch the call's whole weight set into L2 when it fits (<= 96 MB,
+    // under the 129 MB L2 with room for the rest)
+    if (FMT == 1 && rows == 1 && wd != nullptr && sfd != nullptr) {
+        const double per_expert = 3.0 * I * (H / 2.0 + H / 16.0);
+        if (per_expert * topk <= 96.0 * (1 << 20)) {
+            a.l2_prefetch = 1;
+            a.pf_wd = wd;
+            a.pf_sfd = sfd;
+        }
+    }
     return cuda_status(launch_gate_up<FMT>(a, ngroups, cap, s));
 }
 
@@ -266,7 +277,7 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
         } else {
             if ((rc = stage_plan(rows, E, topk, ids_g, w, err, s))) return rc;
             if ((rc = stage_gate_up<FMT>(x_g, rows, H, I, E, topk, ids_g, pg.w, pg.s, pg.sf, pg.s2,
-                                         pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s)))
+                                         pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s, pd.w, pd.sf)))
                 return rc;
             if ((rc = stage_down<FMT>(rows, H, I, E, topk, ids_g, wts_g, pd.w, pd.s, pd.sf, pd.s2,
                                       out_g, w, s)))

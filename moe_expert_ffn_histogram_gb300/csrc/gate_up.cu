@@ -33,6 +33,20 @@ __global__ void __launch_bounds__(kItemThreads, kMinBlocks) gate_up_kernel(const
     __syncthreads();
     pdl_launch_dependents();      // the down kernel may launch; it waits for this grid's results
     if (gv.e < 0) return;
+    if (FMT == 1 && a.l2_prefetch && threadIdx.x == 0) {
+        const int e = gv.e, nfb = gridDim.x, fb = blockIdx.x;
+        const size_t rows = static_cast<size_t>(e) * a.I + static_cast<size_t>(fb) * kFeatBlock;
+        prefetch_l2_range(a.wg + rows * (a.H / 2), static_cast<size_t>(kFeatBlock) * (a.H / 2));
+        prefetch_l2_range(a.wu + rows * (a.H / 2), static_cast<size_t>(kFeatBlock) * (a.H / 2));
+        prefetch_l2_range(a.sfg + rows * (a.H / 16), static_cast<size_t>(kFeatBlock) * (a.H / 16));
+        prefetch_l2_range(a.sfu + rows * (a.H / 16), static_cast<size_t>(kFeatBlock) * (a.H / 16));
+        // this block's 1/nfb share of expert e's down matrix (codes, then scale bytes)
+        const size_t dcodes = static_cast<size_t>(a.H) * (a.I / 2), dsf = static_cast<size_t>(a.H) * (a.I / 16);
+        const size_t c0 = (dcodes * fb / nfb) & ~static_cast<size_t>(15), c1 = (dcodes * (fb + 1) / nfb) & ~static_cast<size_t>(15);
+        const size_t s0 = (dsf * fb / nfb) & ~static_cast<size_t>(15), s1 = (dsf * (fb + 1) / nfb) & ~static_cast<size_t>(15);
+        prefetch_l2_range(a.pf_wd + static_cast<size_t>(e) * dcodes + c0, c1 - c0);
+        prefetch_l2_range(a.pf_sfd + static_cast<size_t>(e) * dsf + s0, s1 - s0);
+    }
     gate_up_item<FMT>(a, gv, blockIdx.x, reinterpret_cast<__half*>(smem_raw), sh);
 }
 

@@ -20,6 +20,12 @@ struct GateUpArgs {
     __half* act;          // [P][I] f16, range-scaled
     float* act_scale;     // [P][I/64] inverse range scale
     int32_t* err;
+    // Single-token NVFP4 calls whose weights fit in L2: each CTA first asks L2 for its own gate/up
+    // rows and for its share of its expert's down matrix (bulk prefetch), so that HBM streams the
+    // whole working set at once while the warps consume it from L2.
+    int l2_prefetch;
+    const uint8_t* pf_wd;  // down codes [E][H][I/2]
+    const uint8_t* pf_sfd; // down scale bytes [E][H][I/16]
 };
 
 // Down projection fused with the slot-order combine (down_combine.cu).

@@ -139,6 +139,16 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Bulk L2 prefetch of [p, p + bytes) in chunks of at most 64 KB; p 16-byte aligned, the tail
+// below 16 bytes is left out.
+__device__ __forceinline__ void prefetch_l2_range(const uint8_t* p, size_t bytes) {
+    bytes &= ~static_cast<size_t>(15);
+    for (size_t o = 0; o < bytes; o += 65536) {
+        const size_t n = bytes - o < 65536 ? bytes - o : 65536;
+        prefetch_l2(p + o, static_cast<uint32_t>(n));
+    }
+}
+
 // Programmatic dependent launch: let the next kernel on the stream start launching, and (in that
 // kernel) wait until every grid it depends on has completed and its writes are visible.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -154,6 +154,34 @@ MOE_API int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int
                       int32_t* err, void* stream);
 
 /*
+ * moe_fp8_forward_layer / moe_nvfp4_forward_layer - the forwards above with the MoE layer's
+ * epilogue fused into the combine: out = bf16(((sum_k w[t,k] * y[t,k]) + shared[t]) + residual[t]),
+ * the two adds in fp32 in that order after the slot-order sum, one rounding
+ * ("spark_model layers/glm5next_mlp/forward.rs", `forward_moe`: the shared expert's output enters
+ * the routed combine, not routed-scaled; the Step gate's full-layer check: final add order
+ * routed-plus-shared-then-residual).
+ *   shared    [T][H] bf16 shared-expert output (e.g. from moe_shared_expert_bf16), or NULL.
+ *   residual  [T][H] bf16 residual stream, or NULL.  Both device pointers, 16-byte aligned, and
+ *             neither may alias out.
+ * Everything else as the forwards above (same workspace size).
+ */
+MOE_API int moe_fp8_forward_layer(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                  const int32_t* topk_ids, const float* topk_weights,
+                                  const uint8_t* w_gate, const float* s_gate,
+                                  const uint8_t* w_up, const float* s_up,
+                                  const uint8_t* w_down, const float* s_down, float limit,
+                                  const uint16_t* shared, const uint16_t* residual, uint16_t* out,
+                                  void* workspace, size_t workspace_bytes, int32_t* err, void* stream);
+MOE_API int moe_nvfp4_forward_layer(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                    const int32_t* topk_ids, const float* topk_weights,
+                                    const uint8_t* w_gate, const uint8_t* sf_gate, float scale2_gate,
+                                    const uint8_t* w_up, const uint8_t* sf_up, float scale2_up,
+                                    const uint8_t* w_down, const uint8_t* sf_down, float scale2_down,
+                                    float limit, const uint16_t* shared, const uint16_t* residual,
+                                    uint16_t* out, void* workspace, size_t workspace_bytes,
+                                    int32_t* err, void* stream);
+
+/*
  * Stage entry points. moe_plan, then moe_*_gate_up, then moe_*_down_combine (on one stream, same
  * workspace, same arguments as the forward they stand for) compute exactly the bits of
  * moe_*_forward for T <= 8, as three separate kernels; moe_*_forward runs the same work items in
@@ -244,6 +272,21 @@ MOE_API int moe_router(const uint16_t* x, int T, int H, const uint16_t* router_w
                        int E, int topk, float routed_scale, int renormalize, float* logits,
                        int32_t* topk_ids, float* topk_weights, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/*
+ * moe_shared_expert_bf16 - the MoE layer's shared expert, a dense BF16 SwiGLU MLP over all tokens
+ * ("spark_model layers/glm5next_mlp/forward.rs", `forward_moe`: `forward_dense` on the shared
+ * weights into `shared_out`; the Step gate's replicated BF16 SwiGLU with its own limit):
+ *   out[t] = bf16( Wd . bf16( silu(min(Wg.x[t], L)) * clamp(Wu.x[t], -L, L) ) ), fp32 accumulation.
+ *   x [T][H] bf16; w_gate, w_up [S][H] bf16; w_down [H][S] bf16; out [T][H] bf16 (device).
+ *   workspace >= moe_shared_expert_workspace_bytes(T, H, S) bytes, 256-byte aligned.
+ * Limits: H, S multiples of 32; limit > 0 (+INFINITY: no clamp); 16-byte aligned arrays. Errors
+ * return synchronously with nothing enqueued; otherwise five launches, no host synchronisation.
+ */
+MOE_API size_t moe_shared_expert_workspace_bytes(int T, int H, int S);
+MOE_API int moe_shared_expert_bf16(const uint16_t* x, int T, int H, int S, const uint16_t* w_gate,
+                                   const uint16_t* w_up, const uint16_t* w_down, float limit,
+                                   uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Library build identification: the compiled CUDA architecture string (e.g. "sm_103a"). */
 MOE_API const char* moe_build_arch(void);

@@ -25,7 +25,8 @@ ERRBIT_BAD_ID = 1
 EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_nvfp4_forward",
             "moe_plan", "moe_fp8_gate_up", "moe_fp8_down_combine", "moe_nvfp4_gate_up",
             "moe_nvfp4_down_combine", "moe_build_arch", "moe_fp8_forward_noalloc",
-            "moe_router_workspace_bytes", "moe_router")
+            "moe_router_workspace_bytes", "moe_router", "moe_fp8_forward_layer",
+            "moe_nvfp4_forward_layer", "moe_shared_expert_workspace_bytes", "moe_shared_expert_bf16")
 
 _lib = None
 
@@ -80,6 +81,16 @@ def load(path: Optional[str] = None):
     lib.moe_router_workspace_bytes.argtypes = [i32, i32, i32]
     lib.moe_router.restype = i32
     lib.moe_router.argtypes = [vp, i32, i32, vp, vp, i32, i32, f32, i32, vp, vp, vp, vp, sz, vp]
+    lib.moe_fp8_forward_layer.restype = i32
+    lib.moe_fp8_forward_layer.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          f32, vp, vp, vp, vp, sz, vp, vp]
+    lib.moe_nvfp4_forward_layer.restype = i32
+    lib.moe_nvfp4_forward_layer.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, vp,
+                                            f32, vp, vp, f32, f32, vp, vp, vp, vp, sz, vp, vp]
+    lib.moe_shared_expert_workspace_bytes.restype = sz
+    lib.moe_shared_expert_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.moe_shared_expert_bf16.restype = i32
+    lib.moe_shared_expert_bf16.argtypes = [vp, i32, i32, i32, vp, vp, vp, f32, vp, vp, sz, vp]
     if path is None:
         _lib = lib
     return lib
@@ -205,6 +216,58 @@ def forward(x, ids, wts, bank, limit: float, **kw):
     if bank.fmt == "fp8":
         return fp8_forward(x, ids, wts, bank, limit, **kw)
     return nvfp4_forward(x, ids, wts, bank, limit, **kw)
+
+
+def forward_layer(x, ids, wts, bank, limit: float, shared=None, residual=None, out=None,
+                  workspace=None, err=None, stream=None):
+    """moe_*_forward_layer: the forward with out = bf16((routed + shared) + residual)."""
+    E, I, _ = bank.w_gate.shape
+    fmt = FMT_FP8 if bank.fmt == "fp8" else FMT_NVFP4
+    dev, T, H, topk, out, ws = _common(x, ids, wts, out, workspace, err, fmt, E, I)
+    for n, t in (("shared", shared), ("residual", residual)):
+        if t is not None:
+            _need(t, n, torch.bfloat16, dev)
+            if tuple(t.shape) != (T, H):
+                raise ValueError(f"{n} must be [T, H]")
+    lib = load()
+    if bank.fmt == "fp8":
+        rc = lib.moe_fp8_forward_layer(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
+                                       _ptr(bank.w_gate), _ptr(bank.s_gate), _ptr(bank.w_up),
+                                       _ptr(bank.s_up), _ptr(bank.w_down), _ptr(bank.s_down),
+                                       float(limit), _ptr(shared), _ptr(residual), _ptr(out), _ptr(ws),
+                                       ws.numel(), _ptr(err), _stream(dev, stream))
+    else:
+        rc = lib.moe_nvfp4_forward_layer(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
+                                         _ptr(bank.w_gate), _ptr(bank.sf_gate), float(bank.scale2_gate),
+                                         _ptr(bank.w_up), _ptr(bank.sf_up), float(bank.scale2_up),
+                                         _ptr(bank.w_down), _ptr(bank.sf_down), float(bank.scale2_down),
+                                         float(limit), _ptr(shared), _ptr(residual), _ptr(out), _ptr(ws),
+                                         ws.numel(), _ptr(err), _stream(dev, stream))
+    _check("moe_*_forward_layer", rc)
+    return out
+
+
+def shared_expert(x, w_gate, w_up, w_down, limit: float, out=None, workspace=None, stream=None):
+    """moe_shared_expert_bf16: dense bf16 SwiGLU MLP, out [T, H] bf16."""
+    dev = x.device
+    _need(x, "x", torch.bfloat16, dev)
+    for n, t in (("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down)):
+        _need(t, n, torch.bfloat16, dev)
+    T, H = x.shape
+    S = w_gate.shape[0]
+    lib = load()
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        n = int(lib.moe_shared_expert_workspace_bytes(T, H, S))
+        if n == 0:
+            raise ValueError("invalid sizes for moe_shared_expert_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    rc = lib.moe_shared_expert_bf16(_ptr(x), T, H, S, _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                    float(limit), _ptr(out), _ptr(workspace), workspace.numel(),
+                                    _stream(dev, stream))
+    _check("moe_shared_expert_bf16", rc)
+    return out
 
 
 # ---- stages (T <= 8), for profiling and interleaving ----------------------------------------------

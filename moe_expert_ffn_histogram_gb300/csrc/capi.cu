@@ -166,7 +166,8 @@ int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, co
 template <int FMT>
 int stage_down(int rows, int H, int I, int E, int topk, const int32_t* ids, const float* wts,
                const uint8_t* wd, const float* sd, const uint8_t* sfd, float s2d, uint16_t* out,
-               const Ws& w, cudaStream_t s) {
+               const Ws& w, cudaStream_t s, const uint16_t* shared = nullptr,
+               const uint16_t* residual = nullptr) {
     DownArgs a{};
     a.T = rows;
     a.H = H;
@@ -183,6 +184,8 @@ int stage_down(int rows, int H, int I, int E, int topk, const int32_t* ids, cons
     a.act = w.at<__half>(w.L.act);
     a.act_scale = w.at<float>(w.L.act_scale);
     a.out = reinterpret_cast<__nv_bfloat16*>(out);
+    a.shared = reinterpret_cast<const __nv_bfloat16*>(shared);
+    a.residual = reinterpret_cast<const __nv_bfloat16*>(residual);
     return cuda_status(launch_down_combine<FMT>(a, s));
 }
 
@@ -192,7 +195,8 @@ int stage_fused(const uint16_t* x, int rows, int H, int I, int E, int topk, cons
                 const float* wts, const uint8_t* wg, const float* sg, const uint8_t* sfg, float s2g,
                 const uint8_t* wu, const float* su, const uint8_t* sfu, float s2u,
                 const uint8_t* wd, const float* sd, const uint8_t* sfd, float s2d, float limit,
-                uint16_t* out, const Ws& w, int32_t* err, cudaStream_t s) {
+                uint16_t* out, const Ws& w, int32_t* err, cudaStream_t s,
+                const uint16_t* shared = nullptr, const uint16_t* residual = nullptr) {
     Groups grp{};
     grp.ids = ids;
     grp.topk = topk;
@@ -230,6 +234,8 @@ int stage_fused(const uint16_t* x, int rows, int H, int I, int E, int topk, cons
     da.act = ga.act;
     da.act_scale = ga.act_scale;
     da.out = reinterpret_cast<__nv_bfloat16*>(out);
+    da.shared = reinterpret_cast<const __nv_bfloat16*>(shared);
+    da.residual = reinterpret_cast<const __nv_bfloat16*>(residual);
     const int cap = rows == 1 ? 1 : fused_cap(rows, topk);
     return cuda_status(launch_fused_forward<FMT>(ga, da, w.at<unsigned>(w.L.barrier), rows, cap, s));
 }
@@ -244,7 +250,8 @@ struct Proj {
 template <int FMT>
 int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32_t* ids,
             const float* wts, Proj pg, Proj pu, Proj pd, float limit, uint16_t* out, void* ws,
-            size_t ws_bytes, int32_t* err, cudaStream_t s) {
+            size_t ws_bytes, int32_t* err, cudaStream_t s, const uint16_t* shared = nullptr,
+            const uint16_t* residual = nullptr) {
     int rc = check_sizes(T, H, I, E, topk);
     if (rc) return rc;
     if (uses_prefill(T, H, I, E, FMT)) {
@@ -254,7 +261,9 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
         PrefillWeights wt{pg.w, pu.w, pd.w, pg.s, pu.s, pd.s, pg.sf, pu.sf, pd.sf, pg.s2, pu.s2, pd.s2};
         return cuda_status(launch_prefill(FMT, reinterpret_cast<const __nv_bfloat16*>(x), T, H, I, E, topk,
                                           ids, wts, wt, limit, reinterpret_cast<__nv_bfloat16*>(out),
-                                          static_cast<uint8_t*>(ws), L, err, s));
+                                          static_cast<uint8_t*>(ws), L, err, s,
+                                          reinterpret_cast<const __nv_bfloat16*>(shared),
+                                          reinterpret_cast<const __nv_bfloat16*>(residual)));
     }
     const int rows_max = rows_per_sweep(T);
     Ws w;
@@ -269,10 +278,12 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
         const float* wts_g = wts + static_cast<size_t>(start) * topk;
         const uint16_t* x_g = x + static_cast<size_t>(start) * H;
         uint16_t* out_g = out + static_cast<size_t>(start) * H;
+        const uint16_t* sh_g = shared ? shared + static_cast<size_t>(start) * H : nullptr;
+        const uint16_t* rs_g = residual ? residual + static_cast<size_t>(start) * H : nullptr;
         if (MOE_FORWARD_FUSED && (rows > 1 || MOE_FORCE_FUSED)) {
             if ((rc = stage_fused<FMT>(x_g, rows, H, I, E, topk, ids_g, wts_g, pg.w, pg.s, pg.sf,
                                        pg.s2, pu.w, pu.s, pu.sf, pu.s2, pd.w, pd.s, pd.sf, pd.s2,
-                                       limit, out_g, w, err, s)))
+                                       limit, out_g, w, err, s, sh_g, rs_g)))
                 return rc;
         } else {
             if ((rc = stage_plan(rows, E, topk, ids_g, w, err, s))) return rc;
@@ -280,7 +291,7 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
                                          pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s, pd.w, pd.sf)))
                 return rc;
             if ((rc = stage_down<FMT>(rows, H, I, E, topk, ids_g, wts_g, pd.w, pd.s, pd.sf, pd.s2,
-                                      out_g, w, s)))
+                                      out_g, w, s, sh_g, rs_g)))
                 return rc;
         }
         start += rows;
@@ -353,6 +364,48 @@ int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
                       Proj{w_up, nullptr, sf_up, scale2_up},
                       Proj{w_down, nullptr, sf_down, scale2_down}, limit, out, workspace,
                       workspace_bytes, err, static_cast<cudaStream_t>(stream));
+}
+
+// ---- the forwards with the layer epilogue ---------------------------------------------------
+
+int moe_fp8_forward_layer(const uint16_t* x, int T, int H, int I, int E, int topk,
+                          const int32_t* topk_ids, const float* topk_weights, const uint8_t* w_gate,
+                          const float* s_gate, const uint8_t* w_up, const float* s_up,
+                          const uint8_t* w_down, const float* s_down, float limit,
+                          const uint16_t* shared, const uint16_t* residual, uint16_t* out,
+                          void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!x || !topk_ids || !topk_weights || !w_gate || !s_gate || !w_up || !s_up || !w_down ||
+        !s_down || !out)
+        return MOE_ERR_NULL;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, w_down, out)) return MOE_ERR_ALIGN;
+    if ((shared && !aligned16(shared)) || (residual && !aligned16(residual))) return MOE_ERR_ALIGN;
+    return forward<0>(x, T, H, I, E, topk, topk_ids, topk_weights, Proj{w_gate, s_gate, nullptr, 1.f},
+                      Proj{w_up, s_up, nullptr, 1.f}, Proj{w_down, s_down, nullptr, 1.f}, limit,
+                      out, workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream), shared,
+                      residual);
+}
+
+int moe_nvfp4_forward_layer(const uint16_t* x, int T, int H, int I, int E, int topk,
+                            const int32_t* topk_ids, const float* topk_weights, const uint8_t* w_gate,
+                            const uint8_t* sf_gate, float scale2_gate, const uint8_t* w_up,
+                            const uint8_t* sf_up, float scale2_up, const uint8_t* w_down,
+                            const uint8_t* sf_down, float scale2_down, float limit,
+                            const uint16_t* shared, const uint16_t* residual, uint16_t* out,
+                            void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!x || !topk_ids || !topk_weights || !w_gate || !sf_gate || !w_up || !sf_up || !w_down ||
+        !sf_down || !out)
+        return MOE_ERR_NULL;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
+    if (!std::isfinite(scale2_gate) || !std::isfinite(scale2_up) || !std::isfinite(scale2_down))
+        return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, w_down, sf_gate, sf_up, sf_down, out)) return MOE_ERR_ALIGN;
+    if ((shared && !aligned16(shared)) || (residual && !aligned16(residual))) return MOE_ERR_ALIGN;
+    return forward<1>(x, T, H, I, E, topk, topk_ids, topk_weights,
+                      Proj{w_gate, nullptr, sf_gate, scale2_gate},
+                      Proj{w_up, nullptr, sf_up, scale2_up},
+                      Proj{w_down, nullptr, sf_down, scale2_down}, limit, out, workspace,
+                      workspace_bytes, err, static_cast<cudaStream_t>(stream), shared, residual);
 }
 
 // ---- stage entry points (T <= 8: one sweep) -------------------------------------------------
@@ -474,6 +527,40 @@ int moe_router(const uint16_t* x, int T, int H, const uint16_t* router_w, const 
                                      reinterpret_cast<const __nv_bfloat16*>(router_w), bias, E, topk, routed_scale,
                                      renormalize != 0, logits, topk_ids, topk_weights, static_cast<float*>(workspace),
                                      ks, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- shared expert ----------------------------------------------------------------------------
+
+namespace {
+bool shared_shape_ok(int T, int H, int S) {
+    return T >= 1 && H >= 32 && S >= 32 && H % 32 == 0 && S % 32 == 0;
+}
+}  // namespace
+
+size_t moe_shared_expert_workspace_bytes(int T, int H, int S) {
+    if (!shared_shape_ok(T, H, S)) return 0;
+    int sms = 0;
+    if (device_sms(&sms) != MOE_OK) sms = 152;
+    return shared_expert_ws_bytes(T, H, S, sms);
+}
+
+int moe_shared_expert_bf16(const uint16_t* x, int T, int H, int S, const uint16_t* w_gate,
+                           const uint16_t* w_up, const uint16_t* w_down, float limit, uint16_t* out,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!x || !w_gate || !w_up || !w_down || !out) return MOE_ERR_NULL;
+    if (!shared_shape_ok(T, H, S)) return MOE_ERR_SHAPE;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, w_down, out)) return MOE_ERR_ALIGN;
+    if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MOE_ERR_WORKSPACE;
+    int sms = 0;
+    int rc = device_sms(&sms);
+    if (rc) return rc;
+    if (workspace_bytes < shared_expert_ws_bytes(T, H, S, sms)) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_shared_expert(
+        reinterpret_cast<const __nv_bfloat16*>(x), T, H, S, reinterpret_cast<const __nv_bfloat16*>(w_gate),
+        reinterpret_cast<const __nv_bfloat16*>(w_up), reinterpret_cast<const __nv_bfloat16*>(w_down), limit,
+        reinterpret_cast<__nv_bfloat16*>(out), static_cast<uint8_t*>(workspace), sms,
+        static_cast<cudaStream_t>(stream)));
 }
 
 const char* moe_build_arch(void) { return "sm_103a"; }

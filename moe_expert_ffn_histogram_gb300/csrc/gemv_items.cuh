@@ -488,7 +488,10 @@ __device__ void down_item(const DownArgs& a, const GroupList& gl, int jt, float*
             if (e < 0 || e >= a.E) continue;
             s = __fadd_rn(s, __fmul_rn(a.wts[p], ys[p * kDownRows + r]));
         }
-        a.out[static_cast<size_t>(t) * H + j0 + r] = __float2bfloat16_rn(s);
+        const size_t o = static_cast<size_t>(t) * H + j0 + r;
+        if (a.shared != nullptr) s = __fadd_rn(s, __bfloat162float(a.shared[o]));
+        if (a.residual != nullptr) s = __fadd_rn(s, __bfloat162float(a.residual[o]));
+        a.out[o] = __float2bfloat16_rn(s);
     }
 }
 

@@ -41,6 +41,9 @@ struct DownArgs {
     const __half* act;      // [P][I]
     const float* act_scale; // [P][I/64]
     __nv_bfloat16* out;     // [T][H]
+    // layer epilogue (nullable): out = bf16((sum_k w*y + shared) + residual), fp32 adds in that order
+    const __nv_bfloat16* shared;     // [T][H] shared-expert output
+    const __nv_bfloat16* residual;   // [T][H]
 };
 
 // FMT: 0 = FP8 E4M3 with 128x128 block scales, 1 = NVFP4.
@@ -74,7 +77,8 @@ struct PrefillWeights {
 cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
                            const int32_t* ids, const float* wts, const PrefillWeights& wt, float limit,
                            __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L, int32_t* err,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const __nv_bfloat16* shared = nullptr,
+                           const __nv_bfloat16* residual = nullptr);
 
 // Router (router.cu): K-split factor for (T, H, E), top-k shared memory, and the two launches.
 int router_ksplit(int T, int H, int E, int sms);
@@ -82,6 +86,16 @@ size_t router_topk_smem_bytes(int E);
 cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloat16* w, const float* bias, int E,
                           int topk, float routed_scale, int renorm, float* logits, int32_t* ids, float* wts,
                           float* part, int KS, cudaStream_t stream);
+
+// Dense bf16 product partials: part[ks][t][n] = sum over K chunk range ks of x[t][:] . w[n][:]
+// (x [T][K], w [N][K], N % 16 == 0, K % 32 == 0; the router's logits kernel).
+cudaError_t launch_dense_bf16(const __nv_bfloat16* x, int T, int K, const __nv_bfloat16* w, int N, float* part,
+                              int KS, cudaStream_t stream);
+// Shared expert (shared_expert.cu): workspace bytes and the launches.
+size_t shared_expert_ws_bytes(int T, int H, int S, int sms);
+cudaError_t launch_shared_expert(const __nv_bfloat16* x, int T, int H, int S, const __nv_bfloat16* wg,
+                                 const __nv_bfloat16* wu, const __nv_bfloat16* wd, float limit,
+                                 __nv_bfloat16* out, uint8_t* ws, int sms, cudaStream_t stream);
 
 // Route histogram / stable counting sort, optionally emitting expert groups (route_plan.cu).
 cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,

@@ -171,7 +171,9 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
                                                               const int32_t* __restrict__ pair_to_sorted,
                                                               const float* __restrict__ wts,
                                                               int topk, int H,
-                                                              __nv_bfloat16* __restrict__ out) {
+                                                              __nv_bfloat16* __restrict__ out,
+                                                              const __nv_bfloat16* __restrict__ shared,
+                                                              const __nv_bfloat16* __restrict__ residual) {
     const int t = blockIdx.x;
     int rows[kMaxTopk];
     float w[kMaxTopk];
@@ -190,6 +192,12 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
             s[1] = __fadd_rn(s[1], __fmul_rn(w[k], v.y));
             s[2] = __fadd_rn(s[2], __fmul_rn(w[k], v.z));
             s[3] = __fadd_rn(s[3], __fmul_rn(w[k], v.w));
+        }
+        const size_t oj = static_cast<size_t>(t) * H + j;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {                 // layer epilogue: (routed + shared) + residual
+            if (shared != nullptr) s[q] = __fadd_rn(s[q], __bfloat162float(shared[oj + q]));
+            if (residual != nullptr) s[q] = __fadd_rn(s[q], __bfloat162float(residual[oj + q]));
         }
         __nv_bfloat162 lo = __floats2bfloat162_rn(s[0], s[1]), hi = __floats2bfloat162_rn(s[2], s[3]);
         uint2 o;
@@ -424,7 +432,7 @@ int gemm_grid() {
 cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
                            const int32_t* ids, const float* wts, const PrefillWeights& wt, float limit,
                            __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L, int32_t* err,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const __nv_bfloat16* shared, const __nv_bfloat16* residual) {
     if (fmt == 1 && MOE_PREFILL_TC != 4) return cudaErrorNotSupported;   // NVFP4: TMEM core only
     const uint8_t *wg = wt.wg, *wu = wt.wu, *wd = wt.wd;
     const float *sg = wt.sg, *su = wt.su, *sd = wt.sd;
@@ -535,7 +543,8 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
         if ((st = cudaGetLastError()) != cudaSuccess) return st;
     }
 
-    prefill_combine_kernel<<<T, 256, 0, stream>>>(f32, I32(L.pair_to_sorted), wts, topk, H, out);
+    prefill_combine_kernel<<<T, 256, 0, stream>>>(f32, I32(L.pair_to_sorted), wts, topk, H, out, shared,
+                                                  residual);
     return cudaGetLastError();
 }
 

@@ -150,18 +150,22 @@ int router_ksplit(int T, int H, int E, int sms) {
     return ks < 1 ? 1 : ks;
 }
 
+cudaError_t launch_dense_bf16(const __nv_bfloat16* x, int T, int K, const __nv_bfloat16* w, int N, float* part,
+                              int KS, cudaStream_t stream) {
+    const int ex = (N / 16 + kRtWarps - 1) / kRtWarps;
+    if (T > 32)
+        router_logits_kernel<4><<<dim3(ex, (T + 31) / 32, KS), kRtWarps * 32, 0, stream>>>(x, T, K, w, N, part);
+    else
+        router_logits_kernel<1><<<dim3(ex, (T + 7) / 8, KS), kRtWarps * 32, 0, stream>>>(x, T, K, w, N, part);
+    return cudaGetLastError();
+}
+
 size_t router_topk_smem_bytes(int E) { return static_cast<size_t>(kRtTopkWarps) * 2 * E * sizeof(float); }
 
 cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloat16* w, const float* bias, int E,
                           int topk, float routed_scale, int renorm, float* logits, int32_t* ids, float* wts,
                           float* part, int KS, cudaStream_t stream) {
-    const int ex = (E / 16 + kRtWarps - 1) / kRtWarps;
-    if (T > 32) {
-        router_logits_kernel<4><<<dim3(ex, (T + 31) / 32, KS), kRtWarps * 32, 0, stream>>>(x, T, H, w, E, part);
-    } else {
-        router_logits_kernel<1><<<dim3(ex, (T + 7) / 8, KS), kRtWarps * 32, 0, stream>>>(x, T, H, w, E, part);
-    }
-    cudaError_t st = cudaGetLastError();
+    cudaError_t st = launch_dense_bf16(x, T, H, w, E, part, KS, stream);
     if (st != cudaSuccess) return st;
     const size_t smem = router_topk_smem_bytes(E);
     if (smem > 48 * 1024 &&

@@ -59,7 +59,8 @@ def _load():
         lib.oracle_hardware_threads.restype = ctypes.c_int
         for name in ("oracle_combine", "oracle_dequant_fp8", "oracle_dequant_nvfp4",
                      "oracle_route_permute", "oracle_moe_fp8", "oracle_moe_nvfp4",
-                     "oracle_router_logits", "oracle_router_topk"):
+                     "oracle_router_logits", "oracle_router_topk", "oracle_shared_expert",
+                     "oracle_layer_epilogue"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -242,3 +243,31 @@ def router_topk(logits: np.ndarray, bias, topk: int, routed_scale: float, renorm
                                     int(bool(renormalize)), _ptr(ids), _ptr(wts))
     assert rc == 0, rc
     return ids, wts
+
+
+# ---- shared expert and the layer epilogue -----------------------------------------------------
+
+def shared_expert(x_bf16_bits, wg_bits, wu_bits, wd_bits, limit: float, nthreads: int = 0) -> np.ndarray:
+    """FP64 dense SwiGLU MLP: x [T][H], wg/wu [S][H], wd [H][S] (bf16 bits) -> [T][H] float64."""
+    x = _c(x_bf16_bits, np.uint16)
+    wg, wu, wd = (_c(a, np.uint16) for a in (wg_bits, wu_bits, wd_bits))
+    T, H = x.shape
+    S = wg.shape[0]
+    out = np.zeros((T, H), np.float64)
+    rc = _load().oracle_shared_expert(_ptr(x), T, H, S, _ptr(wg), _ptr(wu), _ptr(wd),
+                                      ctypes.c_double(limit), _ptr(out), int(nthreads))
+    assert rc == 0, rc
+    return out
+
+
+def layer_epilogue(routed: np.ndarray, shared_bits=None, residual_bits=None):
+    """(float64 sum, bf16 bits) of routed + shared + residual, rounded once."""
+    r = _c(routed, np.float64)
+    sh = None if shared_bits is None else _c(shared_bits, np.uint16)
+    rs = None if residual_bits is None else _c(residual_bits, np.uint16)
+    out = np.zeros(r.shape, np.float64)
+    outb = np.zeros(r.shape, np.uint16)
+    rc = _load().oracle_layer_epilogue(_ptr(r), _ptr(sh), _ptr(rs), ctypes.c_int64(r.size), _ptr(out),
+                                       _ptr(outb))
+    assert rc == 0, rc
+    return out, outb

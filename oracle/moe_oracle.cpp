@@ -423,6 +423,47 @@ int oracle_router_topk(const double* logits, int T, int E, const double* bias, i
     return 0;
 }
 
+// Shared expert in double: out[t] = Wd . (silu(min(Wg.x, L)) * clamp(Wu.x, -L, L)), bf16 weights
+// and x decoded exactly, no intermediate rounding ("spark_model layers/glm5next_mlp/forward.rs",
+// `forward_moe`: `forward_dense` on the shared weights).
+int oracle_shared_expert(const uint16_t* x, int T, int H, int S, const uint16_t* wg, const uint16_t* wu,
+                         const uint16_t* wd, double limit, double* out, int nthreads) {
+    if (T < 1 || H < 1 || S < 1 || !(limit > 0.0)) return -2;
+    std::vector<double> act(static_cast<size_t>(T) * S);
+    parallel_for(static_cast<int64_t>(T) * S, resolve_threads(nthreads), [&](int64_t idx) {
+        const int64_t t = idx / S, n = idx % S;
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            const double xv = bf16_value(x[t * H + h]);
+            g += xv * bf16_value(wg[n * H + h]);
+            u += xv * bf16_value(wu[n * H + h]);
+        }
+        act[idx] = clamped_swiglu(g, u, limit);
+    });
+    parallel_for(static_cast<int64_t>(T) * H, resolve_threads(nthreads), [&](int64_t idx) {
+        const int64_t t = idx / H, j = idx % H;
+        double s = 0.0;
+        for (int n = 0; n < S; ++n) s += act[t * S + n] * bf16_value(wd[j * S + n]);
+        out[idx] = s;
+    });
+    return 0;
+}
+
+// The layer epilogue: out = bf16(routed + shared + residual), exact sum then one rounding
+// (forward.rs `forward_moe`: shared output added in the routed combine; the Step gate's
+// final add order routed-plus-shared-then-residual). shared / residual: bf16 bits, nullable.
+int oracle_layer_epilogue(const double* routed, const uint16_t* shared, const uint16_t* residual, int64_t n,
+                          double* out_f64, uint16_t* out_bf16) {
+    for (int64_t i = 0; i < n; ++i) {
+        double s = routed[i];
+        if (shared) s += bf16_value(shared[i]);
+        if (residual) s += bf16_value(residual[i]);
+        if (out_f64) out_f64[i] = s;
+        if (out_bf16) out_bf16[i] = bf16_round(s);
+    }
+    return 0;
+}
+
 int oracle_hardware_threads(void) { return resolve_threads(0); }
 
 }  // extern "C"

@@ -354,3 +354,34 @@ def test_router_topk_against_sort_and_expit():
         sel = sig[t, order]
         assert np.allclose(w[t], 2.5 * sel / sel.sum(), rtol=1e-12)
     assert ids[3, 0] == 10 and ids[3, 1] == 40
+
+
+# ---- shared expert and the layer epilogue -------------------------------------------------------
+
+def test_shared_expert_against_numpy():
+    from scipy.special import expit
+    g = torch.Generator().manual_seed(21)
+    T, H, S, L = 3, 64, 32, 7.0
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(S, H, generator=g) * 0.3).to(torch.bfloat16)
+    wu = (torch.randn(S, H, generator=g) * 0.3).to(torch.bfloat16)
+    wd = (torch.randn(H, S, generator=g) * 0.2).to(torch.bfloat16)
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    got = oracle.shared_expert(bits(x), bits(wg), bits(wu), bits(wd), L)
+    f = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    gg, uu = f(x) @ f(wg).T, f(x) @ f(wu).T
+    gc = np.minimum(gg, L)
+    a = gc * expit(gc) * np.clip(uu, -L, L)
+    assert np.allclose(got, a @ f(wd).T, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_epilogue_single_rounding():
+    one = lambda v: torch.tensor([v], dtype=torch.bfloat16).view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    s, b = oracle.layer_epilogue(np.array([1.0]), one(0.5), one(0.25))
+    assert s[0] == 1.75 and oracle.bf16_value(int(b[0])) == 1.75
+    # 1 + 2^-9 (+ 2^-9 + 2^-9): one rounding gives 1 + 2^-7; rounding the routed sum first would
+    # give 1 (1 + 2^-8 is a tie that goes to even)
+    s, b = oracle.layer_epilogue(np.array([1.0 + 2 ** -9]), one(2 ** -9), one(2 ** -9))
+    assert oracle.bf16_value(int(b[0])) == 1.0 + 2 ** -7
+    s, b = oracle.layer_epilogue(np.array([-3.0]))
+    assert s[0] == -3.0

@@ -42,9 +42,19 @@ int rows_per_sweep(int T) { return T < kMaxRowsPerSweep ? T : kMaxRowsPerSweep; 
 
 // The grouped-GEMM (prefill) tier: FP8 weights, more than one 8-token sweep, and shapes its
 // tiles cover (per-K-block scale tables of <= 64 entries).
+// Smallest T the grouped-GEMM tier takes; below it, sweeps of <= 8 tokens through the cooperative
+// kernel. Measured on GB300 with the decode banks (uniform routes over 256 / 160 experts, L2
+// flushed): FP8 sweeps win up to T = 24 (1.57 vs 1.69 ms) and lose from T = 32 (2.11 vs
+// 2.02 ms); NVFP4 sweeps win at T = 16 (0.57 vs 0.60 ms) and lose from T = 24 (0.86 vs 0.76 ms).
+#ifndef MOE_PREFILL_MIN_T
+#define MOE_PREFILL_MIN_T 0
+#endif
+constexpr int kGroupedMinRowsFp8 = 28, kGroupedMinRowsFp4 = 18;
+
 bool uses_prefill(int T, int H, int I, int E, int fmt) {
+    const int min_t = MOE_PREFILL_MIN_T > 0 ? MOE_PREFILL_MIN_T : (fmt == 0 ? kGroupedMinRowsFp8 : kGroupedMinRowsFp4);
     // NVFP4 also needs K % 256 == 0 (16-byte loads of 4 slices' scale bytes per row)
-    return T > kMaxRowsPerSweep && H <= 8192 && I <= 8192 && E <= kMaxPlanExperts &&
+    return T > kMaxRowsPerSweep && T >= min_t && H <= 8192 && I <= 8192 && E <= kMaxPlanExperts &&
            static_cast<long long>(T) * kMaxTopk < (1LL << 30) &&
            (fmt == 0 || (H % 256 == 0 && I % 256 == 0));
 }

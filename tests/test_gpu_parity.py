@@ -249,7 +249,7 @@ def test_nvfp4_decode_full_size():
 
 # ---- the grouped-GEMM (prefill) tier: FP8, T > 8 ----------------------------------------------------
 
-@pytest.mark.parametrize("T,H,I,E,routes", [(9, 256, 128, 16, "uniform"), (64, 384, 256, 40, "zipf"),
+@pytest.mark.parametrize("T,H,I,E,routes", [(28, 256, 128, 16, "uniform"), (64, 384, 256, 40, "zipf"),
                                             (300, 256, 256, 8, "uniform"), (130, 512, 384, 24, "zipf")])
 def test_prefill_parity(T, H, I, E, routes):
     wl = inputs.make_custom("fp8", T, H, I, E, seed=700 + T, device=DEV, routes=routes)
@@ -273,14 +273,14 @@ def test_prefill_skewed_and_bad_ids():
 def test_prefill_clamp_stress_and_no_limit():
     wl = inputs.make_custom("fp8", 40, 256, 256, 10, seed=802, device=DEV, x_scale=40.0)
     check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], "prefill clamp stress")
-    wl2 = inputs.make_custom("fp8", 24, 256, 128, 10, seed=803, device=DEV, x_scale=20.0,
+    wl2 = inputs.make_custom("fp8", 30, 256, 128, 10, seed=803, device=DEV, x_scale=20.0,
                              limit=float("inf"))
     check_close(bf16_to_f64(run(wl2)), oracle_for(wl2)["out"], "prefill no limit")
 
 
 # ---- the grouped-GEMM tier over NVFP4 banks (K multiples of 256) -------------------------------------
 
-@pytest.mark.parametrize("T,H,I,E,routes", [(9, 256, 256, 16, "uniform"), (64, 512, 256, 40, "zipf"),
+@pytest.mark.parametrize("T,H,I,E,routes", [(18, 256, 256, 16, "uniform"), (64, 512, 256, 40, "zipf"),
                                             (300, 256, 512, 8, "uniform"), (130, 768, 512, 24, "zipf")])
 def test_nvfp4_prefill_parity(T, H, I, E, routes):
     wl = inputs.make_custom("nvfp4", T, H, I, E, seed=900 + T, device=DEV, routes=routes)
@@ -310,6 +310,13 @@ def test_nvfp4_prefill_full_size_sampled():
     toks = [0, 5, 1000, 2047, 4095]
     res = oracle_for(wl, tokens=toks)
     check_close(bf16_to_f64(out[toks]), res["out"], "nvfp4_prefill sampled")
+
+
+@pytest.mark.parametrize("fmt,T", [("fp8", 27), ("fp8", 28), ("nvfp4", 17), ("nvfp4", 18)])
+def test_tier_crossover_both_sides(fmt, T):
+    """Just below (8-token sweeps) and at (grouped GEMM) the measured crossover width."""
+    wl = inputs.make_custom(fmt, T, 512, 256, 20, seed=950 + T, device=DEV)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"crossover {fmt} T={T}")
 
 
 def test_prefill_bitwise_repeatable():

@@ -303,6 +303,30 @@ def bench_ours(args):
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ev]
 
+    # ---- the same calls captured once per route set in a CUDA graph and replayed
+    graph_ms, graph_err = [], None
+    try:
+        graphs = []
+        for j in range(N_ROUTE_SETS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fwd(sets[j])
+            graphs.append(g)
+        torch.cuda.synchronize()
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            graphs[i % N_ROUTE_SETS].replay()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                graph_ms.append(a_.elapsed_time(b_))
+        del graphs
+    except Exception as exc:                       # report, do not fail the bench line
+        graph_err = f"{type(exc).__name__}: {exc}"[:200]
+        torch.cuda.synchronize()
+
     # ---- the same work as three stage kernels (informational: what fusion saves)
     T = wl0.T
     stage_ms = {"plan": [], "gate_up": [], "down_combine": []}
@@ -437,6 +461,10 @@ def bench_ours(args):
         "stage_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in stage_ms.items() if v},
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,
+        "graph": ({"ms_per_step": round(statistics.mean(graph_ms), 5),
+                   "value": round(T / (statistics.mean(graph_ms) * 1e-3), 2), "unit": UNIT,
+                   "note": "the same forward replayed from a CUDA graph per route set"}
+                  if graph_ms else {"error": graph_err}),
         "router": None if not router_ms else {
             "us": round(statistics.mean(router_ms) * 1e3, 2), "T": T, "E": E, "H": wl0.H,
             "weight_gbs": round(E * wl0.H * 2 / (statistics.mean(router_ms) * 1e-3) / 1e9, 1),

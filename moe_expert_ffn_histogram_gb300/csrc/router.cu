@@ -9,13 +9,14 @@
 //     HBM, no conversion), B = 8 tokens per MMA column tile, mma.sync m16n8k16 bf16 -> f32, with
 //     the lane layout of the FFN kernels (lane c streams 16 bytes of each of its two rows per
 //     32-wide K chunk; elements 4i+{0,1} / 4i+{2,3} are logical K (2c,2c+1) / (2c+8,2c+9) of step
-//     i, and B is read at the same physical positions). Single-token and few-token calls split K
-//     over the grid's z dimension (partial logits in the workspace) so that enough warps stream
-//     the router matrix; wide calls take 32 tokens per CTA so that the matrix is re-read from L2
-//     once per 32 tokens.
-//   router_topk_kernel: one warp per token sums the K parts in order, computes sigmoid and score,
-//     and selects top-k by repeated warp arg-max (score descending, ties to the lower expert
-//     index); weights are the picks' sigmoids (renormalised in pick order, times routed_scale).
+//     i, and B is read at the same physical positions). Few-token calls (T <= 32) take one CTA per
+//     16 rows x 8 tokens x K part (up to 8 parts, summed in order by the consumer); its 16 warps
+//     split the part again and meet in shared memory (dense_small_kernel). Wide calls take 32
+//     tokens per CTA so that the matrix is re-read from L2 once per 32 tokens.
+//   router_topk_kernel: one CTA per token sums the K parts in order and computes sigmoid and score
+//     for every expert; its first warp selects top-k by repeated warp arg-max (score descending,
+//     ties to the lower expert index); weights are the picks' sigmoids (renormalised in pick
+//     order, times routed_scale).
 #include "kernels.cuh"
 
 namespace moe {
@@ -23,7 +24,7 @@ namespace moe {
 namespace {
 
 constexpr int kRtWarps = 4;                       // expert tiles of 16 per logits CTA
-constexpr int kRtTopkWarps = 4;                   // tokens per top-k CTA
+constexpr int kRtTopkWarps = 4;                   // warps of a top-k CTA (one token)
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -79,27 +80,80 @@ __global__ void __launch_bounds__(kRtWarps * 32) router_logits_kernel(const __nv
     }
 }
 
+// Few tokens (T <= 32): one CTA per (16 rows, 8 tokens); its 16 warps split K, keep four 32-wide
+// chunks of loads in flight each, and meet in shared memory (fixed order) - no partial buffer.
+constexpr int kRtSmallWarps = 16;
+__global__ void __launch_bounds__(kRtSmallWarps * 32) dense_small_kernel(const __nv_bfloat16* __restrict__ x, int T,
+                                                                         int H, const __nv_bfloat16* __restrict__ w,
+                                                                         int E, float* __restrict__ out) {
+    __shared__ float red[kRtSmallWarps][32][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int e0 = blockIdx.x * 16, tbase = blockIdx.y * 8;
+    // this CTA's K part (grid z), split again over its 16 warps
+    const int KS = gridDim.z, ks = blockIdx.z, NC = H / 32;
+    const int c0 = ks * NC / KS, nc = (ks + 1) * NC / KS - c0;
+    const int k0 = c0 + warp * nc / kRtSmallWarps, k1 = c0 + (warp + 1) * nc / kRtSmallWarps;
+    const uint4* ra = reinterpret_cast<const uint4*>(w + static_cast<size_t>(e0 + g) * H + c * 8);
+    const uint4* rb = reinterpret_cast<const uint4*>(w + static_cast<size_t>(e0 + g + 8) * H + c * 8);
+    const int t = tbase + g;
+    const bool tv = t < T;
+    const uint4* xb = reinterpret_cast<const uint4*>(x + static_cast<size_t>(tv ? t : 0) * H + c * 8);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int kU = 4;
+    for (int kc = k0; kc < k1; kc += kU) {
+        uint4 qa[kU], qb[kU], bx[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const bool in = kc + u < k1;
+            qa[u] = in ? ld_stream_v4(ra + (kc + u) * 4) : make_uint4(0, 0, 0, 0);
+            qb[u] = in ? ld_stream_v4(rb + (kc + u) * 4) : make_uint4(0, 0, 0, 0);
+            bx[u] = in && tv ? __ldg(xb + (kc + u) * 4) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            mma_bf16(acc, qa[u].x, qb[u].x, qa[u].y, qb[u].y, bx[u].x, bx[u].y);
+            mma_bf16(acc, qa[u].z, qb[u].z, qa[u].w, qb[u].w, bx[u].z, bx[u].w);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) red[warp][lane][q] = acc[q];
+    __syncthreads();
+    if (warp == 0) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int v = 0; v < kRtSmallWarps; ++v)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s[q] += red[v][lane][q];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int tt = tbase + 2 * c + (q & 1), e = e0 + g + 8 * (q >> 1);
+            if (tt < T) out[(static_cast<size_t>(ks) * T + tt) * E + e] = s[q];
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const float* __restrict__ part, int KS,
                                                                         int T, int E, const float* __restrict__ bias,
                                                                         int topk, float routed_scale, int renorm,
                                                                         float* __restrict__ logits,
                                                                         int32_t* __restrict__ ids,
                                                                         float* __restrict__ wts) {
-    extern __shared__ float rt_smem[];                // [warps][2][E]: sigmoid, score
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kRtTopkWarps + warp;
-    if (t >= T) return;
-    float* sig = rt_smem + static_cast<size_t>(warp) * 2 * E;
+    // one CTA per token: all its threads sum the K parts and score the experts, warp 0 selects
+    extern __shared__ float rt_smem[];                // [2][E]: sigmoid, score
+    const int lane = threadIdx.x & 31, t = blockIdx.x;
+    float* sig = rt_smem;
     float* score = sig + E;
-    for (int e = lane; e < E; e += 32) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float l = 0.0f;
+#pragma unroll 8
         for (int q = 0; q < KS; ++q) l += part[(static_cast<size_t>(q) * T + t) * E + e];
         if (logits != nullptr) logits[static_cast<size_t>(t) * E + e] = l;
         const float s = 1.0f / (1.0f + expf(-l));
         sig[e] = s;
         score[e] = s + (bias != nullptr ? bias[e] : 0.0f);
     }
-    __syncwarp();
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
     float picked[kMaxTopk];
     int pid[kMaxTopk];
     for (int k = 0; k < topk; ++k) {
@@ -142,11 +196,12 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const fl
 
 int router_ksplit(int T, int H, int E, int sms) {
     if (T > 32) return 1;
-    const int ctas = ((E / 16 + kRtWarps - 1) / kRtWarps) * ((T + 7) / 8);
-    int ks = (2 * sms + ctas - 1) / ctas;
-    const int nc = H / 32;
-    if (ks > nc / 2) ks = nc / 2;
-    if (ks > 64) ks = 64;
+    // few tokens: enough CTAs (one per 16 rows x 8 tokens x K part) to cover the SMs; each CTA
+    // splits its part again over 16 warps
+    const int ctas = (E / 16) * ((T + 7) / 8);
+    int ks = (sms + ctas - 1) / ctas;
+    if (ks > 8) ks = 8;
+    if (ks > H / 32 / 16) ks = H / 32 / 16;
     return ks < 1 ? 1 : ks;
 }
 
@@ -156,11 +211,11 @@ cudaError_t launch_dense_bf16(const __nv_bfloat16* x, int T, int K, const __nv_b
     if (T > 32)
         router_logits_kernel<4><<<dim3(ex, (T + 31) / 32, KS), kRtWarps * 32, 0, stream>>>(x, T, K, w, N, part);
     else
-        router_logits_kernel<1><<<dim3(ex, (T + 7) / 8, KS), kRtWarps * 32, 0, stream>>>(x, T, K, w, N, part);
+        dense_small_kernel<<<dim3(N / 16, (T + 7) / 8, KS), kRtSmallWarps * 32, 0, stream>>>(x, T, K, w, N, part);
     return cudaGetLastError();
 }
 
-size_t router_topk_smem_bytes(int E) { return static_cast<size_t>(kRtTopkWarps) * 2 * E * sizeof(float); }
+size_t router_topk_smem_bytes(int E) { return static_cast<size_t>(2) * E * sizeof(float); }
 
 cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloat16* w, const float* bias, int E,
                           int topk, float routed_scale, int renorm, float* logits, int32_t* ids, float* wts,
@@ -172,7 +227,7 @@ cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloa
         (st = cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem))) != cudaSuccess)
         return st;
-    router_topk_kernel<<<(T + kRtTopkWarps - 1) / kRtTopkWarps, kRtTopkWarps * 32, smem, stream>>>(
+    router_topk_kernel<<<T, kRtTopkWarps * 32, smem, stream>>>(
         part, KS, T, E, bias, topk, routed_scale, renorm, logits, ids, wts);
     return cudaGetLastError();
 }

@@ -17,9 +17,10 @@
 //                                 prescaled block scale, tcgen05.st into TMEM slot sc % 4;
 //   warps 12-19  epilogue         read D (lane = weight row, column = token) with tcgen05.ld,
 //                                 SwiGLU (gate/up) or the row scales (down), token-major stores;
-//   warp 20      MMA              one thread: per slice and K=16 step one M=128 x N=128 MMA per
-//                                 weight matrix; one commit per slice frees the slot (token box
-//                                 and TMEM slice), one per tile hands the accumulator over.
+//   warp 20      MMA              one thread: per slice and K=16 step one M=128 x N MMA per weight
+//                                 matrix (N = the tile's valid rows rounded up to 16); one commit
+//                                 per slice frees the slot (token box and TMEM slice), one per
+//                                 tile hands the accumulator over.
 // gate/up: NM = 2 (gate rows nt*128.., up rows nt*128..), one accumulator (the two D matrices
 // fill 256 TMEM columns, the four slots the other 256). down: NM = 1 (output rows nt*128..), the
 // K halves of the slice split over the two converter groups, two accumulators so that the
@@ -36,7 +37,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTwSlots = 4;                      // token boxes in smem = weight slices in TMEM
+constexpr int kTwSlotsMax = 8;                   // token boxes in smem = weight slices in TMEM
 constexpr int kTwRawStages = 6;                  // raw E4M3 weight boxes in smem
 constexpr int kTwTok = 128 * 128;                // token slice: 128 rows x 64 f16 (16 KB)
 constexpr int kTwTokWarps = 2;                   // producer warps for token boxes (slots w, w+2)
@@ -53,14 +54,17 @@ struct TwCfg {
     static constexpr int kRowBytes = FMT == 0 ? 64 : 32;   // raw bytes of one row's 64-wide slice
     static constexpr int kRaw = NM * 128 * kRowBytes;      // raw weight boxes of one slice
     // (at least 120 KB, so that one CTA - and one 512-column TMEM allocation - fits per SM)
-    static constexpr int kSmemUsed = kTwSlots * kTwTok + kTwRawStages * kRaw + 1024;
+    // slots: 4 with two weight matrices (their TMEM slices and the accumulator fill 512 columns),
+    // 8 with one
+    static constexpr int kSlots = NM == 2 ? 4 : 8;
+    static constexpr int kSmemUsed = kSlots * kTwTok + kTwRawStages * kRaw + 1024;
     static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
     static constexpr int kAcc = DB ? 2 : 1;                // accumulator buffers
     static constexpr uint32_t kAccCols = NM * 128;         // one buffer: NM matrices x 128 tokens
     static constexpr uint32_t kACols = NM * 32;            // one slot: 64 K (32 f16 pairs) per matrix
     static constexpr uint32_t kA0 = kAcc * kAccCols;       // first A column
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kA0 + kTwSlots * kACols <= kTmemCols, "TMEM budget");
+    static_assert(kA0 + kSlots * kACols <= kTmemCols && kSlots <= kTwSlotsMax && kSlots % 2 == 0, "TMEM budget");
     static_assert(kRaw % 1024 == 0, "stage alignment");
 };
 
@@ -71,7 +75,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     prefill_tw_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ CUtensorMap tmTok,
                            const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1) {
     using Cfg = TwCfg<NM, DB, FMT>;
-    constexpr int NS = kTwSlots, NR = kTwRawStages;
+    constexpr int NS = Cfg::kSlots, NR = kTwRawStages;
     constexpr uint32_t kIdesc128 = idesc_f16_f32<128, 128>();
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -267,6 +271,13 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d0 = tmem + b * Cfg::kAccCols;
+                // MMA width = the tile's valid rows rounded up to 16: the last m-tile of an expert
+                // is often far from full, and the MMA time scales with N
+                int mt, nt;
+                decode_tile(p, tile, mt, nt);
+                const int rows = min(128, p.offsets[p.tile_e[mt] + 1] - p.tile_r0[mt]);
+                const uint32_t n_eff = static_cast<uint32_t>((rows + 15) & ~15);
+                const uint32_t idesc = (kIdesc128 & ~(0x3Fu << 17)) | ((n_eff >> 3) << 17);
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt, ++sc) {
                     const uint32_t s = sc % NS, us = sc / NS;
@@ -282,7 +293,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                         const uint64_t bdesc = smem_desc_sw128(tok + kk * 32);
 #pragma unroll
                         for (int m = 0; m < NM; ++m)
-                            mma_issue_tmem_a(d0 + m * 128, a0 + m * 32 + kk * 8, bdesc, kIdesc128,
+                            mma_issue_tmem_a(d0 + m * 128, a0 + m * 32 + kk * 8, bdesc, idesc,
                                              (kt > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&sempty[s]);

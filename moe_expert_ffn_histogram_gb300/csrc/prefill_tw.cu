@@ -355,7 +355,11 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                     for (int j = 0; j < 16; ++j) {
                         const int t = c0 + j;
                         const float xs = xs_s[ew][t];
-                        const float h = clamped_swiglu(gv[j] * xs * winv0, uv[j] * xs * winv1, p.limit);
+                        // the same clamped SwiGLU with the SFU exponential and divide (a few ulp; the
+                        // epilogue holds the single accumulator, so its length stalls the MMA)
+                        const float gg = fminf(gv[j] * xs * winv0, p.limit);
+                        const float uu = fminf(fmaxf(uv[j] * xs * winv1, -p.limit), p.limit);
+                        const float h = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
                         const uint32_t mb = warp_max_bits(fabsf(h));
                         if (t < vrows) {
                             dst[static_cast<size_t>(t) * p.out_ld] = h;

@@ -71,7 +71,10 @@ int group_cap(int rows, int topk) {
 // of 4 (57 KB at H = 7168) leaves room for two CTAs per SM. An expert picked by more tokens of
 // one sweep becomes several groups (its rows are then read once per group) - rare for sweeps of
 // <= 8 tokens over many experts.
-constexpr int kFusedCap = 4;
+#ifndef MOE_FUSED_CAP
+#define MOE_FUSED_CAP 4
+#endif
+constexpr int kFusedCap = MOE_FUSED_CAP;
 int fused_cap(int rows, int topk) {
     const int c = group_cap(rows, topk);
     return c < kFusedCap ? c : kFusedCap;

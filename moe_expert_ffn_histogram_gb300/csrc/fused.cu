@@ -63,7 +63,10 @@ struct FusedCtl {
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(kItemThreads, kMinBlocks)
+#ifndef MOE_FUSED_MIN_BLOCKS
+#define MOE_FUSED_MIN_BLOCKS kMinBlocks
+#endif
+__global__ void __launch_bounds__(kItemThreads, MOE_FUSED_MIN_BLOCKS)
 fused_forward_kernel(const GateUpArgs ga, const DownArgs da, const FusedCtl ctl) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ GroupList gl;

@@ -177,23 +177,27 @@ def alg_bytes(wl):
                 total=w_gu + w_d + x + out + idw, weights=w_gu + w_d)
 
 
-def kernel_source_sha():
+def kernel_source_sha(files=None):
+    """Hash of the kernel's sources: the listed csrc files (its translation unit and the headers
+    it includes), or every .cu/.cuh file of csrc when no list is given."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_ffn_histogram_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    names = sorted(files) if files else sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    for fn in names:
+        h.update(fn.encode())
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(config, kernel):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on these sources."""
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the kernel's
+    current sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     ent = d.get(config, {}).get(kernel)
-    if not ent or ent.get("source_sha") != kernel_source_sha():
+    if not ent or ent.get("source_sha") != kernel_source_sha(ent.get("files")):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -248,8 +252,8 @@ def cpu_baseline(name, device, budget_s=20.0):
 
 # ---- our arm ---------------------------------------------------------------------------------------
 
-def make_route_sets(name, device, bank, E=None):
-    return [inputs.make_workload(name, device=device, bank=bank, route_set=i, E=E)
+def make_route_sets(name, device, bank, E=None, T=None):
+    return [inputs.make_workload(name, device=device, bank=bank, route_set=i, E=E, T=T)
             for i in range(N_ROUTE_SETS)]
 
 
@@ -269,7 +273,7 @@ def bench_ours(args):
     c = inputs.CONFIGS[name]
     E = c["E"] if args.bank_experts is None else args.bank_experts
     bank = inputs.make_bank(name, dev, experts=None if E == c["E"] else range(E))
-    sets = make_route_sets(name, dev, bank, E)
+    sets = make_route_sets(name, dev, bank, E, args.tokens)
     wl0 = sets[0]
     fmt_code = capi.FMT_FP8 if c["fmt"] == "fp8" else capi.FMT_NVFP4
     ws = capi.alloc_workspace(wl0.T, wl0.H, wl0.I, wl0.E, wl0.topk, fmt_code, dev)
@@ -346,6 +350,18 @@ def bench_ours(args):
             stage_ms["plan"].append(e0.elapsed_time(e1))
             stage_ms["gate_up"].append(e1.elapsed_time(e2))
             stage_ms["down_combine"].append(e2.elapsed_time(e3))
+    # ---- prefill: the library's own per-stage events (moe_stage_timing) around each kernel
+    prefill_stage_ms = {}
+    if T > 8:
+        capi.stage_timing(True)
+        try:
+            for i in range(args.steps):
+                flush.zero_()
+                fwd(sets[i % N_ROUTE_SETS])
+                for k, v in capi.stage_times():
+                    prefill_stage_ms.setdefault(k, []).append(v)
+        finally:
+            capi.stage_timing(False)
     clk = clocks.stop()
 
     # ---- the router in front of the path (informational): a synthetic bf16 router matrix
@@ -431,15 +447,33 @@ def bench_ours(args):
     if T <= 8:
         launches_per_step = 2 if T == 1 else 1
     else:
-        flops = 2.0 * 3 * T * 8 * c["H"] * c["I"]
+        # dominant kernel: the gate/up grouped GEMM (two thirds of the flops), timed by the
+        # library's stage events; every (token, slot) pair is one GEMM row
+        P = T * 8
+        gu_flops = 2.0 * 2 * P * c["H"] * c["I"]
+        dn_flops = 2.0 * P * c["H"] * c["I"]
         tpeak = load_tensor_peak()
-        ach = flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "prefill grouped GEMMs (whole step)",
+        gu_ms = statistics.mean(prefill_stage_ms["gate_up_gemm"])
+        dn_ms = statistics.mean(prefill_stage_ms["down_gemm"])
+        ach = gu_flops / (gu_ms * 1e-3) / 1e12
+        step_tf = (gu_flops + dn_flops) / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "prefill_tw_gemm_kernel (gate/up)",
                 "achieved": round(ach, 1), "peak": tpeak, "peak_kind": "measured bf16 dense burst",
-                "unit": "TFLOP/s", "frac": round(ach / tpeak, 4), "traffic": None,
-                "alg_flops_per_step": flops, "hbm_bytes_per_step": int(mean_total),
-                "hbm_frac": round(mean_total / (ms * 1e-3) / 1e9 / peak, 4),
-                "note": "f16 x f16 -> f32 MMA, same nominal rate as bf16"}
+                "unit": "TFLOP/s", "frac": round(ach / tpeak, 4),
+                "traffic": profiled_traffic(name, "gate_up_gemm"),
+                "alg_flops_per_launch": gu_flops, "avg_launch_us": round(gu_ms * 1e3, 2),
+                "down": {"kernel": "prefill_tw_gemm_kernel (down)", "alg_flops_per_launch": dn_flops,
+                         "avg_launch_us": round(dn_ms * 1e3, 2),
+                         "achieved": round(dn_flops / (dn_ms * 1e-3) / 1e12, 1),
+                         "frac": round(dn_flops / (dn_ms * 1e-3) / 1e12 / tpeak, 4),
+                         "traffic": profiled_traffic(name, "down_gemm")},
+                "step": {"alg_flops": gu_flops + dn_flops, "achieved": round(step_tf, 1),
+                         "frac": round(step_tf / tpeak, 4), "hbm_bytes": int(mean_total),
+                         "hbm_frac": round(mean_total / (ms * 1e-3) / 1e9 / peak, 4),
+                         "stages_us": {k: round(statistics.mean(v) * 1e3, 1)
+                                       for k, v in prefill_stage_ms.items()}},
+                "note": "f16 x f16 -> f32 MMA (same nominal rate as bf16); kernel times from the "
+                        "library's stage events on the launching stream"}
         # route plan, tile list, x prep, gate/up GEMM, activation prep, down GEMM, combine
         launches_per_step = 7
 
@@ -528,6 +562,8 @@ def main(argv=None):
     ap.add_argument("--lib", default=None, help="path of an alternative build of the library")
     ap.add_argument("--bank-experts", type=int, default=None,
                     help="use only the first N experts of the bank (small profiling captures)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count T (small profiling captures)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps, always
     if args.impl == "reference":

@@ -288,6 +288,22 @@ MOE_API int moe_shared_expert_bf16(const uint16_t* x, int T, int H, int S, const
                                    const uint16_t* w_up, const uint16_t* w_down, float limit,
                                    uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Stage timing (tracing, off by default). moe_stage_timing(1) makes every moe_*_forward and
+ * moe_*_forward_layer call record a CUDA event on its stream before each of its stages (kernel
+ * launches) and one after the last; moe_stage_timing(0) stops it. moe_stage_times blocks until
+ * the most recent such call's last event has completed and writes, for its first
+ * min(stages, max_stages) stages, the device time in ms (ms[i]) and a static stage name owned by
+ * the library (names[i], when names != NULL). It returns the number written, 0 when timing is
+ * off or no forward ran since it was switched on, MOE_ERR_NULL for ms == NULL, or MOE_ERR_CUDA.
+ * The events serialise stages that otherwise overlap (programmatic dependent launches), so the
+ * intervals are per-stage device times, and a timed forward can be slightly slower than an
+ * untimed one. At most 63 stages per forward are kept. One process-wide recorder: call from one
+ * host thread at a time.
+ */
+MOE_API int moe_stage_timing(int enable);
+MOE_API int moe_stage_times(float* ms, const char** names, int max_stages);
+
 /* Library build identification: the compiled CUDA architecture string (e.g. "sm_103a"). */
 MOE_API const char* moe_build_arch(void);
 

@@ -26,7 +26,8 @@ EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_
             "moe_plan", "moe_fp8_gate_up", "moe_fp8_down_combine", "moe_nvfp4_gate_up",
             "moe_nvfp4_down_combine", "moe_build_arch", "moe_fp8_forward_noalloc",
             "moe_router_workspace_bytes", "moe_router", "moe_fp8_forward_layer",
-            "moe_nvfp4_forward_layer", "moe_shared_expert_workspace_bytes", "moe_shared_expert_bf16")
+            "moe_nvfp4_forward_layer", "moe_shared_expert_workspace_bytes", "moe_shared_expert_bf16",
+            "moe_stage_timing", "moe_stage_times")
 
 _lib = None
 
@@ -91,6 +92,10 @@ def load(path: Optional[str] = None):
     lib.moe_shared_expert_workspace_bytes.argtypes = [i32, i32, i32]
     lib.moe_shared_expert_bf16.restype = i32
     lib.moe_shared_expert_bf16.argtypes = [vp, i32, i32, i32, vp, vp, vp, f32, vp, vp, sz, vp]
+    lib.moe_stage_timing.restype = i32
+    lib.moe_stage_timing.argtypes = [i32]
+    lib.moe_stage_times.restype = i32
+    lib.moe_stage_times.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), i32]
     if path is None:
         _lib = lib
     return lib
@@ -317,6 +322,21 @@ def down_combine(ids, wts, bank, out, workspace, stream=None):
 
 def build_arch() -> str:
     return load().moe_build_arch().decode()
+
+
+def stage_timing(enable: bool) -> None:
+    """moe_stage_timing: switch per-stage CUDA-event recording of the forward calls on or off."""
+    _check("moe_stage_timing", load().moe_stage_timing(1 if enable else 0))
+
+
+def stage_times(max_stages: int = 64):
+    """moe_stage_times: [(stage name, device ms)] of the most recent timed forward (blocks on it)."""
+    ms = (ctypes.c_float * max_stages)()
+    names = (ctypes.c_char_p * max_stages)()
+    n = load().moe_stage_times(ms, names, max_stages)
+    if n < 0:
+        _check("moe_stage_times", n)
+    return [(names[i].decode(), float(ms[i])) for i in range(n)]
 
 
 def router(x: torch.Tensor, router_w: torch.Tensor, topk: int, routed_scale: float = 1.0,

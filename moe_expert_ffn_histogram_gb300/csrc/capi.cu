@@ -17,6 +17,7 @@
 
 #include "../../include/moe_ffn.h"
 #include "kernels.cuh"
+#include "stage_timing.cuh"
 
 
 using namespace moe;
@@ -267,6 +268,7 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
             const uint16_t* residual = nullptr) {
     int rc = check_sizes(T, H, I, E, topk);
     if (rc) return rc;
+    StageScope timing(s);
     if (uses_prefill(T, H, I, E, FMT)) {
         if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
         const PrefillLayout L = prefill_layout(T, H, I, E, topk);
@@ -294,15 +296,19 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
         const uint16_t* sh_g = shared ? shared + static_cast<size_t>(start) * H : nullptr;
         const uint16_t* rs_g = residual ? residual + static_cast<size_t>(start) * H : nullptr;
         if (MOE_FORWARD_FUSED && (rows > 1 || MOE_FORCE_FUSED)) {
+            stage_mark(s, "fused");
             if ((rc = stage_fused<FMT>(x_g, rows, H, I, E, topk, ids_g, wts_g, pg.w, pg.s, pg.sf,
                                        pg.s2, pu.w, pu.s, pu.sf, pu.s2, pd.w, pd.s, pd.sf, pd.s2,
                                        limit, out_g, w, err, s, sh_g, rs_g)))
                 return rc;
         } else {
+            stage_mark(s, "plan");
             if ((rc = stage_plan(rows, E, topk, ids_g, w, err, s))) return rc;
+            stage_mark(s, "gate_up");
             if ((rc = stage_gate_up<FMT>(x_g, rows, H, I, E, topk, ids_g, pg.w, pg.s, pg.sf, pg.s2,
                                          pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s, pd.w, pd.sf)))
                 return rc;
+            stage_mark(s, "down_combine");
             if ((rc = stage_down<FMT>(rows, H, I, E, topk, ids_g, wts_g, pd.w, pd.s, pd.sf, pd.s2,
                                       out_g, w, s, sh_g, rs_g)))
                 return rc;

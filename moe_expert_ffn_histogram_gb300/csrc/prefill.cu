@@ -22,6 +22,7 @@
 // stays in f16's normal range (one f16 rounding per weight); the power of two is undone in the
 // fp32 epilogue. Products accumulate in fp32.
 #include "prefill.cuh"
+#include "stage_timing.cuh"
 
 // Which grouped-GEMM core the prefill tier launches: 4 = weights in TMEM (prefill_tw.cu),
 // 3 = TMA-fed warp-specialised tcgen05/TMEM (prefill_tma.cu), 2 = cp.async-fed warp-specialised (prefill_ws.cu), 1 = simple tcgen05/TMEM
@@ -439,16 +440,19 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     const int P = T * topk;
     auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
     cudaError_t st;
+    stage_mark(stream, "route_plan");
     if ((st = launch_route_plan(ids, P, E, 1, I32(L.counts), I32(L.offsets), I32(L.sorted_pair),
                                 I32(L.pair_to_sorted), nullptr, nullptr, nullptr, nullptr, err,
                                 stream)) != cudaSuccess)
         return st;
+    stage_mark(stream, "tile_list");
     prefill_tiles_kernel<<<1, 1024, 0, stream>>>(I32(L.counts), I32(L.offsets), E, I32(L.tiles),
                                                  I32(L.tile_e), I32(L.tile_r0), I32(L.tile_first),
                                                  I32(L.tile_cnt));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
     float* xinv = reinterpret_cast<float*>(ws + L.xinv);
+    stage_mark(stream, "x_prep");
     prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv,
                                                   MOE_PREFILL_TC >= 3 ? I32(L.pair_to_sorted) : nullptr, topk);
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
@@ -494,6 +498,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     gu.sf1 = wt.sfu;
     gu.s2_0 = wt.s2g;
     gu.s2_1 = wt.s2u;
+    stage_mark(stream, "gate_up_gemm");
     if (MOE_PREFILL_TC == 4) {
         if ((st = launch_prefill_gemm_tw(0, gu, I, stream)) != cudaSuccess) return st;
     } else if (MOE_PREFILL_TC == 3) {
@@ -509,6 +514,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
 
     __half* a16 = reinterpret_cast<__half*>(ws + L.a16);
     float* ainv = reinterpret_cast<float*>(ws + L.ainv);
+    stage_mark(stream, "act_prep");
     prefill_act_prep_kernel<<<P, 256, 0, stream>>>(f32, amax, I32(L.offsets) + E, I, a16, ainv);
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
 
@@ -530,6 +536,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     dn.amax = nullptr;
     dn.out_ld = H;
     dn.a_rows = P;
+    stage_mark(stream, "down_gemm");
     if (MOE_PREFILL_TC == 4) {
         if ((st = launch_prefill_gemm_tw(1, dn, H, stream)) != cudaSuccess) return st;
     } else if (MOE_PREFILL_TC == 3) {
@@ -543,6 +550,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
         if ((st = cudaGetLastError()) != cudaSuccess) return st;
     }
 
+    stage_mark(stream, "combine");
     prefill_combine_kernel<<<T, 256, 0, stream>>>(f32, I32(L.pair_to_sorted), wts, topk, H, out, shared,
                                                   residual);
     return cudaGetLastError();

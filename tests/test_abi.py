@@ -156,3 +156,8 @@ def test_router_rejects_bad_arguments(lib):
     assert call(ws=None) == -3
     assert lib.moe_router_workspace_bytes(2, 250, 64) == 0
     assert lib.moe_router_workspace_bytes(2, 256, 64) > 0
+
+
+def test_stage_times_without_timing(lib):
+    assert lib.moe_stage_times(None, None, 4) == -1
+    assert capi.stage_times() == []            # timing off: nothing recorded

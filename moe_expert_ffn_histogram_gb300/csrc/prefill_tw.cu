@@ -3,28 +3,34 @@
 // Each GEMM is computed transposed: D[weight row][token] = W x A^T, with the weight slice (f16,
 // produced by the converter warps) as the MMA's A operand in TMEM and 128 sorted activation rows
 // (TMA, 128-byte swizzled) as its B operand in shared memory. Dequantised weights thus never
-// pass through shared memory: per 64-wide K slice shared memory carries the token box, the raw
-// E4M3 box and its one read by the converters - the f16 round trip through shared memory is what
-// bounded the core that staged the dequantised weights there (prefill_tma.cu).
-//   warps 0-1    token producers  slice sc -> slot sc % 4 (TMA box 128 rows x 64 f16), once the
-//                                 slot's previous MMAs are done;
-//   warps 2-3    raw producers    slice sc -> raw stage sc % 6 (NM boxes of 128 rows x 64 E4M3
-//                                 bytes, 64-byte swizzled), once the converters have read it;
+// pass through shared memory: per 128-wide K slice shared memory carries the token boxes, the
+// raw weight boxes and their one read by the converters - the f16 round trip through shared
+// memory is what bounded the core that staged the dequantised weights there (prefill_tma.cu).
+//   warps 0-1    token producers  slice sc -> slot sc % NS (two TMA boxes of 128 rows x 64 f16),
+//                                 once the slot's previous MMAs are done;
+//   warps 2-3    raw producers    slice sc -> raw stage sc % NR (per weight matrix one box of 128
+//                                 rows x 128 E4M3 bytes, 128-byte swizzle, or x 64 bytes of packed
+//                                 E2M1 codes, 64-byte swizzle), once the converters have read it;
 //   warps 4-11   converters       warp w writes TMEM lanes 32*(w%4)..+31 (the hardware's lane
 //                                 quarter), lane = weight row; warps 4-7 take matrix (or K half) 0,
 //                                 warps 8-11 matrix (or K half) 1. Read the raw row slice into
 //                                 registers, release the raw stage, dequantise to f16 pairs x
-//                                 prescaled block scale, tcgen05.st into TMEM slot sc % 4;
+//                                 prescaled block scale, tcgen05.st into TMEM slot sc % NS;
 //   warps 12-19  epilogue         read D (lane = weight row, column = token) with tcgen05.ld,
 //                                 SwiGLU (gate/up) or the row scales (down), token-major stores;
 //   warp 20      MMA              one thread: per slice and K=16 step one M=128 x N MMA per weight
 //                                 matrix (N = the tile's valid rows rounded up to 16); one commit
-//                                 per slice frees the slot (token box and TMEM slice), one per
-//                                 tile hands the accumulator over.
+//                                 per slice frees its token boxes and TMEM slice, one per tile
+//                                 hands the accumulator over. No memory access in its loop;
+//   warp 21      watcher          waits on the slice's mbarriers for the MMA warp and releases it
+//                                 through a named barrier (per tile a reduction that carries N).
 // gate/up: NM = 2 (gate rows nt*128.., up rows nt*128..), one accumulator (the two D matrices
-// fill 256 TMEM columns, the four slots the other 256). down: NM = 1 (output rows nt*128..), the
-// K halves of the slice split over the two converter groups, two accumulators so that the
-// epilogue overlaps the next tile.
+// fill 256 TMEM columns, two slots of 2 x 64 columns the other 256). down: NM = 1 (output rows
+// nt*128..), the K halves of the slice split over the two converter groups, two accumulators so
+// that the epilogue overlaps the next tile, four slots of 64 columns.
+// The slice is 128 wide because every slice costs the converters, the watcher and the MMA warp
+// a fixed round of barrier traffic (~500 cycles measured for an empty pipeline of this shape);
+// 128-wide slices double the MMA work that pays for it.
 // Every wait is bounded (~1 s of SM clock); on a timeout the CTA sets bit 1 of the error word,
 // every role leaves its loop, and the CTA frees its TMEM and exits.
 #include <cuda.h>
@@ -33,39 +39,64 @@
 #include "prefill.cuh"
 #include "tc_ptx.cuh"
 
+#ifndef MOE_TW_CE_GU
+#define MOE_TW_CE_GU 1
+#endif
+#ifndef MOE_TW_CE_DN
+#define MOE_TW_CE_DN 1
+#endif
+
 namespace moe {
 
 namespace {
 
-constexpr int kTwSlotsMax = 8;                   // token boxes in smem = weight slices in TMEM
-constexpr int kTwRawStages = 6;                  // raw E4M3 weight boxes in smem
-constexpr int kTwTok = 128 * 128;                // token slice: 128 rows x 64 f16 (16 KB)
-constexpr int kTwTokWarps = 2;                   // producer warps for token boxes (slots w, w+2)
-constexpr int kTwRawWarps = 2;                   // producer warps for raw boxes (stages w, w+2, w+4)
+// Bounded mbarrier wait of this core's pipeline roles.
+__device__ __forceinline__ bool tw_wait(uint64_t* m, uint32_t parity) {
+    if (mbar_test(m, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(m, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+constexpr int kTwSliceK = 128;                   // K per slice
+constexpr int kTwSlotsMax = 4;                   // token slots in smem = weight slices in TMEM
+constexpr int kTwBox = 128 * 128;                // one token box: 128 rows x 64 f16 (16 KB)
+constexpr int kTwTok = 2 * kTwBox;               // token slice: 128 rows x 128 f16 (32 KB)
+constexpr int kTwTokWarps = 2;                   // producer warps for token boxes (odd / even slices)
+constexpr int kTwRawWarps = 2;                   // producer warps for raw boxes (odd / even slices)
 constexpr int kTwConvWarp0 = kTwTokWarps + kTwRawWarps;    // 4
 constexpr int kTwConvWarps = 8;
 constexpr int kTwEpiWarp0 = kTwConvWarp0 + kTwConvWarps;   // 12
 constexpr int kTwEpiWarps = 8;
 constexpr int kTwMmaWarp = kTwEpiWarp0 + kTwEpiWarps;      // 20
-constexpr int kTwThreads = 32 * (kTwMmaWarp + 1);          // 672
+constexpr int kTwWatchWarp = kTwMmaWarp + 1;               // 21
+constexpr int kTwThreads = 32 * (kTwWatchWarp + 1);        // 704
+constexpr uint32_t kTwIssueBar = 1;                        // named barrier: watcher <-> MMA warp
 
 template <int NM, int DB, int FMT>
 struct TwCfg {
-    static constexpr int kRowBytes = FMT == 0 ? 64 : 32;   // raw bytes of one row's 64-wide slice
+    static constexpr int kRowBytes = FMT == 0 ? 128 : 64;  // raw bytes of one row's 128-wide slice
     static constexpr int kRaw = NM * 128 * kRowBytes;      // raw weight boxes of one slice
-    // (at least 120 KB, so that one CTA - and one 512-column TMEM allocation - fits per SM)
-    // slots: 4 with two weight matrices (their TMEM slices and the accumulator fill 512 columns),
-    // 8 with one
-    static constexpr int kSlots = NM == 2 ? 4 : 8;
-    static constexpr int kSmemUsed = kSlots * kTwTok + kTwRawStages * kRaw + 1024;
+    // slots: 2 with two weight matrices (their TMEM slices and the accumulator fill 512 columns),
+    // 4 with one
+    static constexpr int kSlots = NM == 2 ? 2 : 4;
+    // raw stages: as many as fit beside the token slots (at least 120 KB in all, so that one CTA
+    // - and one 512-column TMEM allocation - fits per SM)
+    static constexpr int kRawStages = (NM == 2 && FMT == 0) ? 4 : (NM == 1 && FMT == 0) ? 5 : 6;
+    static constexpr int kCommitSlices = NM == 2 ? MOE_TW_CE_GU : MOE_TW_CE_DN;
+    static constexpr int kSmemUsed = kSlots * kTwTok + kRawStages * kRaw + 1024;
     static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
     static constexpr int kAcc = DB ? 2 : 1;                // accumulator buffers
     static constexpr uint32_t kAccCols = NM * 128;         // one buffer: NM matrices x 128 tokens
-    static constexpr uint32_t kACols = NM * 32;            // one slot: 64 K (32 f16 pairs) per matrix
+    static constexpr uint32_t kMCols = kTwSliceK / 2;      // one matrix's slice: 128 K = 64 f16 pairs
+    static constexpr uint32_t kACols = NM * kMCols;        // one slot
     static constexpr uint32_t kA0 = kAcc * kAccCols;       // first A column
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kA0 + kSlots * kACols <= kTmemCols && kSlots <= kTwSlotsMax && kSlots % 2 == 0, "TMEM budget");
-    static_assert(kRaw % 1024 == 0, "stage alignment");
+    static_assert(kA0 + kSlots * kACols <= kTmemCols && kSlots <= kTwSlotsMax, "TMEM budget");
+    static_assert(kSlots % kCommitSlices == 0, "slot groups");
+    static_assert(kSmemUsed + 6 * 1024 <= 227 * 1024, "shared memory");
+    static_assert(kRaw % 1024 == 0 && kTwTok % 1024 == 0, "stage alignment");
 };
 
 }  // namespace
@@ -75,20 +106,21 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     prefill_tw_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ CUtensorMap tmTok,
                            const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1) {
     using Cfg = TwCfg<NM, DB, FMT>;
-    constexpr int NS = Cfg::kSlots, NR = kTwRawStages;
+    constexpr int NS = Cfg::kSlots, NR = Cfg::kRawStages, CE = Cfg::kCommitSlices;
     constexpr uint32_t kIdesc128 = idesc_f16_f32<128, 128>();
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    // tfull[s]: token box s landed; rfull/rempty[r]: raw box r landed / read by all converters;
-    // afull[s]: weight slice s in TMEM; sempty[s]: the MMAs of slot s (token box and TMEM slice)
-    // are done; acc_full/acc_empty[b]: accumulator b complete / drained.
+    // tfull[s]: token boxes of slot s landed; rfull/rempty[r]: raw boxes r landed / read by all
+    // converters; afull[s]: weight slice s in TMEM; sempty[g]: the MMAs of slot group g (slots
+    // g*CE..+CE-1: their token boxes and TMEM slices) are done; acc_full/acc_empty[b]:
+    // accumulator b complete / drained.
     __shared__ __align__(8) uint64_t tfull[NS], afull[NS], sempty[NS], rfull[NR], rempty[NR], acc_full[2], acc_empty[2];
     __shared__ uint32_t w_scale[kTwConvWarps][64];       // per converter warp: its rows' scale table
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int K = p.K, KT = K / 64, KB = K / 128;
+    const int K = p.K, KT = K / kTwSliceK, KB = K / 128;
     const int total = p.tiles[0] * p.n_tiles;
     auto stTok = [&](uint32_t s) { return smem + s * kTwTok; };
     auto stRaw = [&](uint32_t r) { return smem + NS * kTwTok + r * Cfg::kRaw; };
@@ -97,7 +129,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(&tfull[s], 1);
             mbar_init(&afull[s], kTwConvWarps);
-            mbar_init(&sempty[s], 1);
+            if (s < NS / CE) mbar_init(&sempty[s], 1);
         }
         for (int r = 0; r < NR; ++r) {
             mbar_init(&rfull[r], 1);
@@ -108,7 +140,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             mbar_init(&acc_empty[b], kTwEpiWarps);
         }
         abort_s = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;");
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base_s, Cfg::kTmemCols);
@@ -121,10 +153,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
 
     if (warp < kTwConvWarp0) {
         // ---------------- producers ----------------
-        // Warps 0-1 issue token boxes (slice sc by warp sc % 2 into slot sc % 4, once the slot's
+        // Warps 0-1 issue token boxes (slice sc by warp sc % 2 into slot sc % NS, once the slot's
         // previous MMAs are done); warps 2-3 issue raw weight boxes (slice sc by warp 2 + sc % 2
-        // into raw stage sc % 6, once all converters have read its previous box). Each warp
-        // always serves the same slots / stages, in order.
+        // into raw stage sc % NR, once all converters have read its previous boxes).
         if (lane == 0) {
             const bool tok = warp < kTwTokWarps;
             const int pw = tok ? warp : warp - kTwTokWarps;
@@ -139,15 +170,17 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                     if (static_cast<int>(sc % 2) != pw) continue;
                     if (tok) {
                         const uint32_t s = sc % NS, u = sc / NS;
-                        if (u > 0 && !mbar_wait(&sempty[s], (u - 1) & 1u)) {
+                        if (u > 0 && !tw_wait(&sempty[s / CE], (u - 1) & 1u)) {
                             ok = false;
                             break;
                         }
+                        // rows past the expert's last row are loaded and never used
                         mbar_arrive_expect_tx(&tfull[s], kTwTok);
-                        tma_load_2d(smem_u32(stTok(s)), &tmTok, kt * 64, r0, &tfull[s]);   // rows past the expert: unused
+                        tma_load_2d(smem_u32(stTok(s)), &tmTok, kt * kTwSliceK, r0, &tfull[s]);
+                        tma_load_2d(smem_u32(stTok(s)) + kTwBox, &tmTok, kt * kTwSliceK + 64, r0, &tfull[s]);
                     } else {
                         const uint32_t r = sc % NR, u = sc / NR;
-                        if (u > 0 && !mbar_wait(&rempty[r], (u - 1) & 1u)) {
+                        if (u > 0 && !tw_wait(&rempty[r], (u - 1) & 1u)) {
                             ok = false;
                             break;
                         }
@@ -167,20 +200,23 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     } else if (warp < kTwEpiWarp0) {
         // ---------------- converters ----------------
         // Lane quarter qd = warp % 4 (TMEM access rule); part 0/1 = matrix (NM = 2) or K half
-        // (NM = 1). Eight consecutive lanes read eight consecutive raw rows of one 16-byte chunk,
-        // which the 64-byte swizzle places in eight distinct bank groups. The raw box is
-        // released as soon as it is in registers; the TMEM slot is waited for only then.
+        // (NM = 1). A thread converts its row's slice in pieces of 64 K (32 f16 pairs, one
+        // 32-column TMEM store each): two pieces per matrix slice with NM = 2, its K half with
+        // NM = 1. Raw rows: FP8 128 bytes in 16-byte chunks, 128-byte swizzle (chunk ^ row % 8);
+        // NVFP4 64 bytes of packed codes, 64-byte swizzle (chunk ^ (row / 2) % 4). Eight
+        // consecutive lanes read eight consecutive rows of one chunk, which the swizzle places in
+        // eight distinct bank groups. The raw boxes are released once the last piece is in
+        // registers; the TMEM slot is waited for only before the first store.
         const int cw = warp - kTwConvWarp0, qd = warp & 3, part = cw / 4;
         const int rrow = (NM == 2 ? part * 128 : 0) + 32 * qd + lane;       // raw row of this thread
         const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
-        // FP8: 16-byte chunks of 16 codes, 64-byte rows, 64-byte swizzle. NVFP4: 16-byte chunks of
-        // 32 codes, 32-byte rows, 32-byte swizzle (chunk ^ bit 2 of the row).
-        constexpr int kChunks = FMT == 0 ? (NM == 2 ? 4 : 2) : (NM == 2 ? 2 : 1);
-        const int c0 = NM == 2 ? 0 : kChunks * part;
-        const int sw = FMT == 0 ? (rrow >> 1) & 3 : (rrow >> 2) & 1;
+        constexpr int kPieces = NM == 2 ? 2 : 1;                  // 64-K pieces per thread
+        constexpr int kPieceChunks = FMT == 0 ? 4 : 2;            // 16-byte chunks per piece
+        const int c0 = NM == 2 ? 0 : kPieceChunks * part;         // first chunk of this thread
+        const int sw = FMT == 0 ? (rrow & 7) : ((rrow >> 1) & 3);
         uint32_t* tbl = w_scale[cw];
         const uint8_t* sfrow = nullptr;                    // NVFP4: this row's scale bytes
-        uint4 sfv = make_uint4(0, 0, 0, 0);                // NVFP4: scale bytes of 4 slices (K 256)
+        uint4 sfv = make_uint4(0, 0, 0, 0);                // NVFP4: scale bytes of 2 slices (K 256)
         uint32_t sc = 0;
         for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x) {
             int mt, nt;
@@ -198,57 +234,64 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             bool ok = true;
             for (int kt = 0; kt < KT; ++kt, ++sc) {
                 const uint32_t r = sc % NR, ur = sc / NR, s = sc % NS, us = sc / NS;
-                if (FMT == 1 && (kt & 3) == 0) sfv = __ldg(reinterpret_cast<const uint4*>(sfrow + kt * 4));
-                if (!__all_sync(0xffffffffu, mbar_wait(&rfull[r], ur & 1u))) {
+                if (FMT == 1 && (kt & 1) == 0) sfv = __ldg(reinterpret_cast<const uint4*>(sfrow + kt * 8));
+                if (!__all_sync(0xffffffffu, tw_wait(&rfull[r], ur & 1u))) {
                     ok = false;
                     break;
                 }
                 const uint8_t* raw = stRaw(r) + rrow * Cfg::kRowBytes;
-                uint4 wr[kChunks];
+                const uint32_t ta = tmem + lane_off + Cfg::kA0 + s * Cfg::kACols + (NM == 2 ? part * Cfg::kMCols : part * 32);
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) wr[c] = lds128(raw + (((c0 + c) ^ sw) << 4));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&rempty[r]);
-                if (!__all_sync(0xffffffffu, us == 0 || mbar_wait(&sempty[s], (us - 1) & 1u))) {
-                    ok = false;
-                    break;
-                }
-                uint32_t h[NM == 2 ? 32 : 16];
-                if constexpr (FMT == 0) {
-                    const uint32_t sc2 = tbl[kt >> 1];
+                for (int pc = 0; pc < kPieces; ++pc) {
+                    // the piece's chunks; after the last piece's loads the raw boxes are released
+                    uint4 wr[kPieceChunks];
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        const uint32_t wv[4] = {wr[c].x, wr[c].y, wr[c].z, wr[c].w};
+                    for (int c = 0; c < kPieceChunks; ++c)
+                        wr[c] = lds128(raw + (((c0 + pc * kPieceChunks + c) ^ sw) << 4));
+                    if (pc == kPieces - 1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&rempty[r]);
+                    }
+                    uint32_t h[32];
+                    if constexpr (FMT == 0) {
+                        const uint32_t sc2 = tbl[kt];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t lo, hi;
-                            e4m3x4_to_f16x2x2(wv[i], lo, hi);
-                            h[8 * c + 2 * i] = hmul2(lo, sc2);
-                            h[8 * c + 2 * i + 1] = hmul2(hi, sc2);
+                        for (int c = 0; c < kPieceChunks; ++c) {
+                            const uint4 q = wr[c];
+                            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint32_t lo, hi;
+                                e4m3x4_to_f16x2x2(wv[i], lo, hi);
+                                h[8 * c + 2 * i] = hmul2(lo, sc2);
+                                h[8 * c + 2 * i + 1] = hmul2(hi, sc2);
+                            }
+                        }
+                    } else {
+                        // the piece's 4 scale bytes (one per 16 codes); E2M1 x E4M3 products are exact
+                        const int wsel = (kt & 1) * 2 + (NM == 2 ? pc : part);
+                        const uint32_t sfw = wsel == 0 ? sfv.x : wsel == 1 ? sfv.y : wsel == 2 ? sfv.z : sfv.w;
+#pragma unroll
+                        for (int c = 0; c < kPieceChunks; ++c) {
+                            const uint4 q = wr[c];
+                            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint32_t sf2 = e4m3_splat_f16x2((sfw >> (8 * (2 * c + (i >> 1)))) & 0xFFu);
+                                uint32_t qq[4];
+                                e2m1x8_to_f16x2x4(wv[i], qq[0], qq[1], qq[2], qq[3]);
+#pragma unroll
+                                for (int b = 0; b < 4; ++b) h[16 * c + 4 * i + b] = hmul2(qq[b], sf2);
+                            }
                         }
                     }
-                } else {
-                    // the slice's 4 scale bytes (one per 16 codes); E2M1 x E4M3 products are exact
-                    const uint32_t sfw = (kt & 2) ? ((kt & 1) ? sfv.w : sfv.z) : ((kt & 1) ? sfv.y : sfv.x);
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        const uint32_t wv[4] = {wr[c].x, wr[c].y, wr[c].z, wr[c].w};
-                        const int grp0 = 2 * (c0 + c);     // scale group of the chunk's first 16 codes
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint32_t sf2 = e4m3_splat_f16x2((sfw >> (8 * (grp0 + (i >> 1)))) & 0xFFu);
-                            uint32_t q[4];
-                            e2m1x8_to_f16x2x4(wv[i], q[0], q[1], q[2], q[3]);
-#pragma unroll
-                            for (int b = 0; b < 4; ++b) h[16 * c + 4 * i + b] = hmul2(q[b], sf2);
-                        }
+                    if (pc == 0 && !__all_sync(0xffffffffu, us == 0 || tw_wait(&sempty[s / CE], (us - 1) & 1u))) {
+                        ok = false;
+                        break;
                     }
+                    tmem_st32(ta + pc * 32, h);
                 }
-                const uint32_t ta = tmem + lane_off + Cfg::kA0 + s * Cfg::kACols + (NM == 2 ? part * 32 : part * 16);
-                if constexpr (NM == 2)
-                    tmem_st32(ta, h);
-                else
-                    tmem_st16(ta, h);
+                if (!ok) break;
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -261,50 +304,83 @@ __global__ void __launch_bounds__(kTwThreads, 1)
         }
     } else if (warp == kTwMmaWarp) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            uint32_t sc = 0, tcount = 0;
-            for (int tile = blockIdx.x; tile < total && !abort_s; tile += gridDim.x, ++tcount) {
-                const uint32_t b = tcount % Cfg::kAcc, v = tcount / Cfg::kAcc;
-                if (v > 0 && !mbar_wait(&acc_empty[b], (v - 1) & 1u)) {
-                    abort_s = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d0 = tmem + b * Cfg::kAccCols;
-                // MMA width = the tile's valid rows rounded up to 16: the last m-tile of an expert
-                // is often far from full, and the MMA time scales with N
-                int mt, nt;
-                decode_tile(p, tile, mt, nt);
-                const int rows = min(128, p.offsets[p.tile_e[mt] + 1] - p.tile_r0[mt]);
-                const uint32_t n_eff = static_cast<uint32_t>((rows + 15) & ~15);
-                const uint32_t idesc = (kIdesc128 & ~(0x3Fu << 17)) | ((n_eff >> 3) << 17);
-                bool ok = true;
-                for (int kt = 0; kt < KT; ++kt, ++sc) {
-                    const uint32_t s = sc % NS, us = sc / NS;
-                    if (!mbar_wait(&tfull[s], us & 1u) || !mbar_wait(&afull[s], us & 1u)) {
-                        ok = false;
-                        break;
-                    }
+        // Lane 0 issues. This warp touches no memory in its loop: a shared-memory access (an
+        // mbarrier wait included) by the issuing thread waits for the MMAs queued before it,
+        // i.e. drains the tensor pipe (measured: ~290 instead of ~70 cycles per M=128 MMA).
+        // The watcher warp waits for each slice's operands instead and releases this warp
+        // through named barrier kTwIssueBar: per tile one reduction whose result is the tile's
+        // MMA width / 16 (0: stop), then a plain barrier per further slice (a reduction per
+        // slice costs ~250 cycles more than a plain barrier and starves the pipe).
+        uint32_t sc = 0, tcount = 0;
+        while (true) {
+            const uint32_t n16 = bar_red_popc(kTwIssueBar, 64, false);
+            if (n16 == 0) break;
+            const uint32_t b = tcount % Cfg::kAcc;
+            const uint32_t d0 = tmem + b * Cfg::kAccCols;
+            // MMA width = the tile's valid rows rounded up to 16
+            const uint32_t idesc = (kIdesc128 & ~(0x3Fu << 17)) | ((2u * n16) << 17);
+            for (int kt = 0; kt < KT; ++kt, ++sc) {
+                if (kt > 0) named_bar_sync(kTwIssueBar, 64);
+                if (lane == 0) {
+                    const uint32_t s = sc % NS;
                     tc_fence_after();
                     const uint32_t tok = smem_u32(stTok(s));
                     const uint32_t a0 = tmem + Cfg::kA0 + s * Cfg::kACols;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bdesc = smem_desc_sw128(tok + kk * 32);
+                    for (int kk = 0; kk < kTwSliceK / 16; ++kk) {
+                        // K16 step kk: token box kk / 4, 32-byte column group kk % 4 of its rows
+                        const uint64_t bdesc = smem_desc_sw128(tok + (kk >> 2) * kTwBox + (kk & 3) * 32);
 #pragma unroll
                         for (int m = 0; m < NM; ++m)
-                            mma_issue_tmem_a(d0 + m * 128, a0 + m * 32 + kk * 8, bdesc, idesc,
+                            mma_issue_tmem_a(d0 + m * 128, a0 + m * Cfg::kMCols + kk * 8, bdesc, idesc,
                                              (kt > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(&sempty[s]);
+                    if (s % CE == CE - 1) mma_commit(&sempty[s / CE]);
                     if (kt == KT - 1) mma_commit(&acc_full[b]);
                 }
-                if (!ok) {
-                    abort_s = 1;
-                    break;
+            }
+            ++tcount;
+        }
+    } else if (warp == kTwWatchWarp) {
+        // ---------------- watcher ----------------
+        // Per slice: the accumulator drained (first slice of a tile), the token boxes landed and
+        // the weight slice in TMEM; then the release of the MMA warp - the tile's first slice
+        // by a reduction carrying the MMA width (lanes < n16 vote true; 0 on a timeout or an
+        // abort), every further slice by a plain barrier. After a failed wait the rest of the
+        // tile is released without waiting (the MMA warp cannot be stopped inside a tile; its
+        // results are discarded with the error bit) and the next reduction stops it. A final 0
+        // ends the MMA warp's loop.
+        uint32_t sc = 0, tcount = 0;
+        bool ok = true;
+        bool live = true;                                  // the MMA warp is still in its loop
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
+            int mt, nt;
+            decode_tile(p, tile, mt, nt);
+            const int rows = min(128, p.offsets[p.tile_e[mt] + 1] - p.tile_r0[mt]);
+            const int n16 = (rows + 15) >> 4;              // >= 1: a tile has at least one row
+            const uint32_t b = tcount % Cfg::kAcc, v = tcount / Cfg::kAcc;
+            for (int kt = 0; kt < KT; ++kt, ++sc) {
+                const uint32_t s = sc % NS, us = sc / NS;
+                if (lane == 0 && ok) {
+                    ok = !abort_s;
+                    if (ok && kt == 0 && v > 0) ok = tw_wait(&acc_empty[b], (v - 1) & 1u);
+                    if (ok) ok = tw_wait(&tfull[s], us & 1u) && tw_wait(&afull[s], us & 1u);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (kt == 0) {
+                    if (bar_red_popc(kTwIssueBar, 64, ok && lane < n16) == 0) {
+                        live = false;                      // the MMA warp has left its loop
+                        break;
+                    }
+                } else {
+                    named_bar_sync(kTwIssueBar, 64);
                 }
             }
         }
+        // every release the MMA warp waits for is sent: a final 0 unless a reduction already
+        // returned 0 (then both warps left their loops at the same barrier)
+        if (live) bar_red_popc(kTwIssueBar, 64, false);
+        if (!ok && lane == 0) abort_s = 1;
     } else {
         // ---------------- epilogue ----------------
         // Warp w reads TMEM lanes 32*(w%4)..+31 (lane = weight row f of the tile's slab) and token
@@ -455,11 +531,11 @@ cudaError_t launch_prefill_gemm_tw(int kind, const PrefillGemmArgs& p, int N_tot
     const bool fp4 = p.fmt == 1;
     if (fp4 && ((reinterpret_cast<uintptr_t>(p.sf0) | reinterpret_cast<uintptr_t>(p.sf1)) & 15u))
         return cudaErrorMisalignedAddress;
-    // FP8: rows of K code bytes, boxes of 64 bytes (64-byte swizzle); NVFP4: rows of K/2 bytes of
-    // packed codes, boxes of 32 bytes (32-byte swizzle)
+    // FP8: rows of K code bytes, boxes of 128 bytes (128-byte swizzle); NVFP4: rows of K/2 bytes
+    // of packed codes, boxes of 64 bytes (64-byte swizzle): one 128-wide K slice of 128 rows
     const uint64_t wbytes = fp4 ? p.K / 2 : p.K;
-    const uint32_t wbox = fp4 ? 32 : 64;
-    const CUtensorMapSwizzle wsw = fp4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const uint32_t wbox = fp4 ? 64 : 128;
+    const CUtensorMapSwizzle wsw = fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     const bool ok = tw_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.a, p.K, p.a_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
                     tw_map(&mw0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w0, wbytes, wrows_all, wbox, wsw) &&
                     tw_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w1, wbytes, wrows_all, wbox, wsw);

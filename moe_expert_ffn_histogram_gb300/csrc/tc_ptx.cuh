@@ -121,6 +121,20 @@ __device__ __forceinline__ void mma_issue_tmem_a(uint32_t d_tmem, uint32_t a_tme
         ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// Named barrier over `nthreads` threads (whole warps). A barrier, not a memory access.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named-barrier reduction over `nthreads` threads (whole warps): every participant receives the
+// number of participants whose `pred` is true. A barrier, not a memory access.
+__device__ __forceinline__ uint32_t bar_red_popc(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.popc.u32 %0, %2, %3, p;\n\t}"
+                 : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads) : "memory");
+    return r;
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* m) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(smem_u32(m)) : "memory");

@@ -6,8 +6,8 @@
 // pass through shared memory: per 128-wide K slice shared memory carries the token boxes, the
 // raw weight boxes and their one read by the converters - the f16 round trip through shared
 // memory is what bounded the core that staged the dequantised weights there (prefill_tma.cu).
-//   warps 0-1    token producers  slice sc -> slot sc % NS (two TMA boxes of 128 rows x 64 f16),
-//                                 once the slot's previous MMAs are done;
+//   warps 0-1    token producers  slice sc -> token slot sc % NT (two TMA boxes of 128 rows x 64
+//                                 f16), once the slot's previous MMAs are done;
 //   warps 2-3    raw producers    slice sc -> raw stage sc % NR (per weight matrix one box of 128
 //                                 rows x 128 E4M3 bytes, 128-byte swizzle, or x 64 bytes of packed
 //                                 E2M1 codes, 64-byte swizzle), once the converters have read it;
@@ -19,9 +19,10 @@
 //   warps 12-19  epilogue         read D (lane = weight row, column = token) with tcgen05.ld,
 //                                 SwiGLU (gate/up) or the row scales (down), token-major stores;
 //   warp 20      MMA              one thread: per slice and K=16 step one M=128 x N MMA per weight
-//                                 matrix (N = the tile's valid rows rounded up to 16); one commit
-//                                 per slice frees its token boxes and TMEM slice, one per tile
-//                                 hands the accumulator over. No memory access in its loop;
+//                                 matrix (N = the tile's valid rows rounded up to 16); a commit
+//                                 per slice frees its TMEM slice (and with its own token slots a
+//                                 second one its token boxes), one per tile hands the accumulator
+//                                 over. No memory access in its loop;
 //   warp 21      watcher          waits on the slice's mbarriers for the MMA warp and releases it
 //                                 through a named barrier (per tile a reduction that carries N).
 // gate/up: NM = 2 (gate rows nt*128.., up rows nt*128..), one accumulator (the two D matrices
@@ -45,6 +46,9 @@
 #ifndef MOE_TW_CE_DN
 #define MOE_TW_CE_DN 1
 #endif
+#ifndef MOE_TW_EPI_SPIN
+#define MOE_TW_EPI_SPIN 0
+#endif
 
 namespace moe {
 
@@ -60,7 +64,7 @@ __device__ __forceinline__ bool tw_wait(uint64_t* m, uint32_t parity) {
 }
 
 constexpr int kTwSliceK = 128;                   // K per slice
-constexpr int kTwSlotsMax = 4;                   // token slots in smem = weight slices in TMEM
+constexpr int kTwSlotsMax = 4;                   // token slots in smem / weight slices in TMEM
 constexpr int kTwBox = 128 * 128;                // one token box: 128 rows x 64 f16 (16 KB)
 constexpr int kTwTok = 2 * kTwBox;               // token slice: 128 rows x 128 f16 (32 KB)
 constexpr int kTwTokWarps = 2;                   // producer warps for token boxes (odd / even slices)
@@ -81,11 +85,16 @@ struct TwCfg {
     // slots: 2 with two weight matrices (their TMEM slices and the accumulator fill 512 columns),
     // 4 with one
     static constexpr int kSlots = NM == 2 ? 2 : 4;
+    // token slots: with two weight matrices more than TMEM slots (their own release barrier,
+    // a second commit per slice), so that the token boxes are loaded ahead of the slot
+    // recycling; with one matrix one per TMEM slot (released with it)
+    static constexpr int kTokSlots = NM == 2 ? (FMT == 0 ? 3 : 4) : kSlots;
+    static constexpr bool kTokOwn = kTokSlots != kSlots;
     // raw stages: as many as fit beside the token slots (at least 120 KB in all, so that one CTA
     // - and one 512-column TMEM allocation - fits per SM)
-    static constexpr int kRawStages = (NM == 2 && FMT == 0) ? 4 : (NM == 1 && FMT == 0) ? 5 : 6;
+    static constexpr int kRawStages = (NM == 2 && FMT == 0) ? 3 : (NM == 1 && FMT == 0) ? 5 : (NM == 2) ? 5 : 6;
     static constexpr int kCommitSlices = NM == 2 ? MOE_TW_CE_GU : MOE_TW_CE_DN;
-    static constexpr int kSmemUsed = kSlots * kTwTok + kRawStages * kRaw + 1024;
+    static constexpr int kSmemUsed = kTokSlots * kTwTok + kRawStages * kRaw + 1024;
     static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
     static constexpr int kAcc = DB ? 2 : 1;                // accumulator buffers
     static constexpr uint32_t kAccCols = NM * 128;         // one buffer: NM matrices x 128 tokens
@@ -93,7 +102,7 @@ struct TwCfg {
     static constexpr uint32_t kACols = NM * kMCols;        // one slot
     static constexpr uint32_t kA0 = kAcc * kAccCols;       // first A column
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kA0 + kSlots * kACols <= kTmemCols && kSlots <= kTwSlotsMax, "TMEM budget");
+    static_assert(kA0 + kSlots * kACols <= kTmemCols && kSlots <= kTwSlotsMax && kTokSlots <= kTwSlotsMax, "TMEM budget");
     static_assert(kSlots % kCommitSlices == 0, "slot groups");
     static_assert(kSmemUsed + 6 * 1024 <= 227 * 1024, "shared memory");
     static_assert(kRaw % 1024 == 0 && kTwTok % 1024 == 0, "stage alignment");
@@ -106,15 +115,17 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     prefill_tw_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ CUtensorMap tmTok,
                            const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1) {
     using Cfg = TwCfg<NM, DB, FMT>;
-    constexpr int NS = Cfg::kSlots, NR = Cfg::kRawStages, CE = Cfg::kCommitSlices;
+    constexpr int NS = Cfg::kSlots, NT = Cfg::kTokSlots, NR = Cfg::kRawStages, CE = Cfg::kCommitSlices;
     constexpr uint32_t kIdesc128 = idesc_f16_f32<128, 128>();
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    // tfull[s]: token boxes of slot s landed; rfull/rempty[r]: raw boxes r landed / read by all
-    // converters; afull[s]: weight slice s in TMEM; sempty[g]: the MMAs of slot group g (slots
-    // g*CE..+CE-1: their token boxes and TMEM slices) are done; acc_full/acc_empty[b]:
+    // tfull[t]: token boxes of token slot t landed; tempty[t]: its MMAs are done (own token
+    // slots only); rfull/rempty[r]: raw boxes r landed / read by all converters; afull[s]: weight
+    // slice s in TMEM; sempty[g]: the MMAs of slot group g (slots g*CE..+CE-1: their TMEM slices,
+    // and their token boxes when those are not on their own) are done; acc_full/acc_empty[b]:
     // accumulator b complete / drained.
-    __shared__ __align__(8) uint64_t tfull[NS], afull[NS], sempty[NS], rfull[NR], rempty[NR], acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t tfull[NT], tempty[NT], afull[NS], sempty[NS], rfull[NR], rempty[NR], acc_full[2],
+        acc_empty[2];
     __shared__ uint32_t w_scale[kTwConvWarps][64];       // per converter warp: its rows' scale table
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
@@ -123,11 +134,14 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     const int K = p.K, KT = K / kTwSliceK, KB = K / 128;
     const int total = p.tiles[0] * p.n_tiles;
     auto stTok = [&](uint32_t s) { return smem + s * kTwTok; };
-    auto stRaw = [&](uint32_t r) { return smem + NS * kTwTok + r * Cfg::kRaw; };
+    auto stRaw = [&](uint32_t r) { return smem + NT * kTwTok + r * Cfg::kRaw; };
 
     if (tid == 0) {
+        for (int t = 0; t < NT; ++t) {
+            mbar_init(&tfull[t], 1);
+            mbar_init(&tempty[t], 1);
+        }
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&tfull[s], 1);
             mbar_init(&afull[s], kTwConvWarps);
             if (s < NS / CE) mbar_init(&sempty[s], 1);
         }
@@ -169,8 +183,8 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 for (int kt = 0; kt < KT; ++kt, ++sc) {
                     if (static_cast<int>(sc % 2) != pw) continue;
                     if (tok) {
-                        const uint32_t s = sc % NS, u = sc / NS;
-                        if (u > 0 && !tw_wait(&sempty[s / CE], (u - 1) & 1u)) {
+                        const uint32_t s = sc % NT, u = sc / NT;
+                        if (u > 0 && !tw_wait(Cfg::kTokOwn ? &tempty[s] : &sempty[s / CE], (u - 1) & 1u)) {
                             ok = false;
                             break;
                         }
@@ -322,9 +336,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             for (int kt = 0; kt < KT; ++kt, ++sc) {
                 if (kt > 0) named_bar_sync(kTwIssueBar, 64);
                 if (lane == 0) {
-                    const uint32_t s = sc % NS;
+                    const uint32_t s = sc % NS, t = sc % NT;
                     tc_fence_after();
-                    const uint32_t tok = smem_u32(stTok(s));
+                    const uint32_t tok = smem_u32(stTok(t));
                     const uint32_t a0 = tmem + Cfg::kA0 + s * Cfg::kACols;
 #pragma unroll
                     for (int kk = 0; kk < kTwSliceK / 16; ++kk) {
@@ -336,6 +350,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                                              (kt > 0 || kk > 0) ? 1u : 0u);
                     }
                     if (s % CE == CE - 1) mma_commit(&sempty[s / CE]);
+                    if (Cfg::kTokOwn) mma_commit(&tempty[t]);
                     if (kt == KT - 1) mma_commit(&acc_full[b]);
                 }
             }
@@ -360,11 +375,11 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             const int n16 = (rows + 15) >> 4;              // >= 1: a tile has at least one row
             const uint32_t b = tcount % Cfg::kAcc, v = tcount / Cfg::kAcc;
             for (int kt = 0; kt < KT; ++kt, ++sc) {
-                const uint32_t s = sc % NS, us = sc / NS;
+                const uint32_t s = sc % NS, us = sc / NS, t = sc % NT, ut = sc / NT;
                 if (lane == 0 && ok) {
                     ok = !abort_s;
                     if (ok && kt == 0 && v > 0) ok = tw_wait(&acc_empty[b], (v - 1) & 1u);
-                    if (ok) ok = tw_wait(&tfull[s], us & 1u) && tw_wait(&afull[s], us & 1u);
+                    if (ok) ok = tw_wait(&tfull[t], ut & 1u) && tw_wait(&afull[s], us & 1u);
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (kt == 0) {
@@ -413,7 +428,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             }
             __syncwarp();
             const uint32_t b = tcount % Cfg::kAcc, v = tcount / Cfg::kAcc;
-            if (!__all_sync(0xffffffffu, mbar_wait_sleep(&acc_full[b], v & 1u))) {
+            if (!__all_sync(0xffffffffu, MOE_TW_EPI_SPIN ? tw_wait(&acc_full[b], v & 1u) : mbar_wait_sleep(&acc_full[b], v & 1u))) {
                 abort_s = 1;
                 break;
             }

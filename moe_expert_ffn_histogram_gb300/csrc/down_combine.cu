@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(kItemThreads, kDownMinBlocks) down_combine_ker
     extern __shared__ __align__(16) float ys[];     // [P][16]
     __shared__ GroupList gl;
     load_group_list(a.grp, gl);
-    down_item<FMT, MOE_PDL != 0>(a, gl, blockIdx.x, ys);
+    down_item<FMT, MOE_PDL != 0, FMT == 0 ? kDownBatch : kDownBatchFp4>(a, gl, blockIdx.x, ys);
 }
 
 template <int FMT>

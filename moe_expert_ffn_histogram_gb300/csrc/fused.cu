@@ -117,7 +117,7 @@ fused_forward_kernel(const GateUpArgs ga, const DownArgs da, const FusedCtl ctl)
 
     // ---- phase 2: down + slot-order combine items (16 output rows each) ----
     for (int jt = blockIdx.x; jt < n2; jt += gridDim.x) {
-        down_item<FMT>(da, gl, jt, reinterpret_cast<float*>(smem_raw));
+        down_item<FMT, false, FMT == 0 ? kFusedDownBatch : kFusedDownBatchFp4>(da, gl, jt, reinterpret_cast<float*>(smem_raw));
         __syncthreads();
     }
 }

@@ -32,6 +32,15 @@ constexpr int kMaxPairs = kMaxTopk * kMaxCols;   // pairs of one sub-batch (<= 8
 #ifndef MOE_DN_BATCH
 #define MOE_DN_BATCH 4
 #endif
+#ifndef MOE_DN_BATCH_FP4
+#define MOE_DN_BATCH_FP4 2
+#endif
+#ifndef MOE_FUSED_DN_BATCH
+#define MOE_FUSED_DN_BATCH 1
+#endif
+#ifndef MOE_FUSED_DN_BATCH_FP4
+#define MOE_FUSED_DN_BATCH_FP4 4
+#endif
 #ifndef MOE_MIN_BLOCKS
 #define MOE_MIN_BLOCKS 2
 #endif
@@ -40,7 +49,13 @@ constexpr int kMaxPairs = kMaxTopk * kMaxCols;   // pairs of one sub-batch (<= 8
 #endif
 constexpr int kStagesFp8 = MOE_GU_BATCH;      // 128-wide K blocks per load batch (128 B per row each)
 constexpr int kStagesFp4 = MOE_GU_BATCH_FP4;  // 128-wide K super-segments per batch (64 B per row each)
-constexpr int kDownBatch = MOE_DN_BATCH;      // 64-wide K segments per down load batch
+// 64-wide K segments per down load batch: the stage kernel's (FP8, NVFP4) and the fused kernel's
+// (measured: single-token NVFP4 down 26.0 -> 19.3 us with 2 instead of 4; the fused FP8 batch-M
+// step 400 -> 346 us with 1; the fused NVFP4 step at T=8 best with 4)
+constexpr int kDownBatch = MOE_DN_BATCH;
+constexpr int kDownBatchFp4 = MOE_DN_BATCH_FP4;
+constexpr int kFusedDownBatch = MOE_FUSED_DN_BATCH;
+constexpr int kFusedDownBatchFp4 = MOE_FUSED_DN_BATCH_FP4;
 constexpr int kMinBlocks = MOE_MIN_BLOCKS;    // CTAs per SM the register budget is sized for
 constexpr int kDownMinBlocks = MOE_DN_MIN_BLOCKS;   // the same, for the down stage kernel
 
@@ -323,7 +338,7 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
 // With kWaitDeps (the stage kernel launched as a programmatic dependent of the gate/up kernel),
 // each thread issues its first weight batch BEFORE waiting for the gate/up grid, so the down
 // weight stream starts while the gate/up kernel drains.
-template <int FMT, bool kWaitDeps = false>
+template <int FMT, bool kWaitDeps = false, int kStages = kDownBatch>
 __device__ void down_item(const DownArgs& a, const GroupList& gl, int jt, float* ys) {
     bool waited = false;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -331,7 +346,6 @@ __device__ void down_item(const DownArgs& a, const GroupList& gl, int jt, float*
     const int H = a.H, I = a.I;
     const int j0 = jt * kDownRows;
     const int nseg = I / 64;
-    constexpr int kStages = kDownBatch;
 
     for (int gi = warp; gi < gl.count; gi += kItemWarps) {
         const GroupView& gv = gl.g[gi];

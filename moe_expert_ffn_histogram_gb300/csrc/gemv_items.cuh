@@ -38,6 +38,12 @@ constexpr int kMaxPairs = kMaxTopk * kMaxCols;   // pairs of one sub-batch (<= 8
 #ifndef MOE_FUSED_DN_BATCH
 #define MOE_FUSED_DN_BATCH 1
 #endif
+#ifndef MOE_FUSED_GU_BATCH
+#define MOE_FUSED_GU_BATCH MOE_GU_BATCH
+#endif
+#ifndef MOE_FUSED_GU_BATCH_FP4
+#define MOE_FUSED_GU_BATCH_FP4 MOE_GU_BATCH_FP4
+#endif
 #ifndef MOE_FUSED_DN_BATCH_FP4
 #define MOE_FUSED_DN_BATCH_FP4 4
 #endif
@@ -49,6 +55,8 @@ constexpr int kMaxPairs = kMaxTopk * kMaxCols;   // pairs of one sub-batch (<= 8
 #endif
 constexpr int kStagesFp8 = MOE_GU_BATCH;      // 128-wide K blocks per load batch (128 B per row each)
 constexpr int kStagesFp4 = MOE_GU_BATCH_FP4;  // 128-wide K super-segments per batch (64 B per row each)
+constexpr int kFusedStagesFp8 = MOE_FUSED_GU_BATCH;       // the same in the fused kernel
+constexpr int kFusedStagesFp4 = MOE_FUSED_GU_BATCH_FP4;
 // 64-wide K segments per down load batch: the stage kernel's (FP8, NVFP4) and the fused kernel's
 // (measured: single-token NVFP4 down 26.0 -> 19.3 us with 2 instead of 4; the fused FP8 batch-M
 // step 400 -> 346 us with 1; the fused NVFP4 step at T=8 best with 4)
@@ -103,7 +111,7 @@ __host__ __device__ inline size_t down_item_smem(int rows, int topk) {
 }
 
 // ---- gate + up + SwiGLU for (group gv, feature block fb) --------------------------------------
-template <int FMT>
+template <int FMT, int kSF8 = kStagesFp8, int kSF4 = kStagesFp4>
 __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, __half* xs,
                              GateUpShared& sh) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -183,10 +191,10 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
         const size_t srow = (static_cast<size_t>(e) * (I / 128) + (fb * kFeatBlock) / 128) * (H / 128);
         const float* sgr = a.sg + srow;
         const float* sur = a.su + srow;
-        for (int kb0 = 0; kb0 < nkb; kb0 += kStagesFp8) {
-            uint4 q[kStagesFp8][4];
+        for (int kb0 = 0; kb0 < nkb; kb0 += kSF8) {
+            uint4 q[kSF8][4];
 #pragma unroll
-            for (int s = 0; s < kStagesFp8; ++s) {
+            for (int s = 0; s < kSF8; ++s) {
                 if (kb0 + s < nkb) {
                     const size_t off = static_cast<size_t>(kb0 + s) * 128;
                     q[s][0] = ld_stream_v4(pg + off);
@@ -196,7 +204,7 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
                 }
             }
 #pragma unroll
-            for (int s = 0; s < kStagesFp8; ++s) {
+            for (int s = 0; s < kSF8; ++s) {
                 const int kb = kb0 + s;
                 if (kb < nkb) {
                     float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -236,11 +244,11 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
         const __half* xb4 = xs + static_cast<size_t>(has_b ? g : 0) * H + c * 32;
         const int nsup = H / 128;
         const int sf_shift = 16 * (c & 1);
-        for (int t0 = 0; t0 < nsup; t0 += kStagesFp4) {
-            uint4 qg[kStagesFp4], qu[kStagesFp4];
-            uint2 fg[kStagesFp4], fu[kStagesFp4];
+        for (int t0 = 0; t0 < nsup; t0 += kSF4) {
+            uint4 qg[kSF4], qu[kSF4];
+            uint2 fg[kSF4], fu[kSF4];
 #pragma unroll
-            for (int s = 0; s < kStagesFp4; ++s) {
+            for (int s = 0; s < kSF4; ++s) {
                 if (t0 + s < nsup) {
                     qg[s] = ld_stream_v4(pg + (t0 + s) * 64);
                     qu[s] = ld_stream_v4(pu + (t0 + s) * 64);
@@ -249,7 +257,7 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
                 }
             }
 #pragma unroll
-            for (int s = 0; s < kStagesFp4; ++s) {
+            for (int s = 0; s < kSF4; ++s) {
                 const int t = t0 + s;
                 if (t < nsup) {
                     uint4 bq[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),

@@ -63,7 +63,7 @@ size_t fused_smem_bytes(int H, int rows, int topk, int cap);
 // Wide tier (prefill.cu): workspace layout and the launch sequence of the grouped-GEMM path.
 struct PrefillLayout {
     size_t counts, offsets, sorted_pair, pair_to_sorted, tiles, tile_e, tile_r0, tile_first, tile_cnt;
-    size_t x16, xinv, amax, a16, ainv, f32, total;
+    size_t x16, xinv, amax, a16, ainv, f32, plan_blk, total;
 };
 PrefillLayout prefill_layout(int T, int H, int I, int E, int topk);
 // Weights of the three projections for the prefill tier: FP8 codes + fp32 block scales, or
@@ -102,6 +102,12 @@ cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t
                               int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,
                               int32_t* group_count, int32_t* group_expert, int32_t* group_start,
                               int32_t* group_ncols, int32_t* err, cudaStream_t stream);
+// The same permutation (no groups) over several blocks for many pairs; blk is scratch of
+// route_plan_wide_ws_bytes(P, E) bytes (route_plan.cu). Three launches.
+size_t route_plan_wide_ws_bytes(int P, int E);
+cudaError_t launch_route_plan_wide(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
+                                   int32_t* sorted_pair, int32_t* pair_to_sorted, int32_t* blk,
+                                   int32_t* err, cudaStream_t stream);
 size_t route_plan_smem_bytes(int E);
 
 }  // namespace moe

@@ -394,6 +394,9 @@ __global__ void __launch_bounds__(prefill::kThreads, 2) prefill_gemm_kernel(cons
 
 // ---- workspace and launch sequence ------------------------------------------------------------------
 
+// pairs from which the prefill tier plans its permutation over several blocks
+constexpr int kWidePlanPairs = 4096;
+
 PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     const size_t P = static_cast<size_t>(T) * topk;
     const size_t mtiles = P / prefill::kBM + static_cast<size_t>(E) + 1;
@@ -415,6 +418,7 @@ PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     L.a16 = take(P * static_cast<size_t>(I) * 2);
     L.ainv = take(P * 4);
     L.f32 = take(P * static_cast<size_t>(H > I ? H : I) * 4);   // a (fp32), later y
+    L.plan_blk = take(route_plan_wide_ws_bytes(static_cast<int>(P), E));
     L.total = o;
     return L;
 }
@@ -441,10 +445,14 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
     cudaError_t st;
     stage_mark(stream, "route_plan");
-    if ((st = launch_route_plan(ids, P, E, 1, I32(L.counts), I32(L.offsets), I32(L.sorted_pair),
-                                I32(L.pair_to_sorted), nullptr, nullptr, nullptr, nullptr, err,
-                                stream)) != cudaSuccess)
-        return st;
+    // many pairs: the multi-block plan (one block serialises ~32 rounds of 1024 pairs)
+    if (P >= kWidePlanPairs)
+        st = launch_route_plan_wide(ids, P, E, I32(L.counts), I32(L.offsets), I32(L.sorted_pair),
+                                    I32(L.pair_to_sorted), I32(L.plan_blk), err, stream);
+    else
+        st = launch_route_plan(ids, P, E, 1, I32(L.counts), I32(L.offsets), I32(L.sorted_pair),
+                               I32(L.pair_to_sorted), nullptr, nullptr, nullptr, nullptr, err, stream);
+    if (st != cudaSuccess) return st;
     stage_mark(stream, "tile_list");
     prefill_tiles_kernel<<<1, 1024, 0, stream>>>(I32(L.counts), I32(L.offsets), E, I32(L.tiles),
                                                  I32(L.tile_e), I32(L.tile_r0), I32(L.tile_first),

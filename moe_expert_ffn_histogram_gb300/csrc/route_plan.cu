@@ -148,6 +148,117 @@ route_plan_kernel(const int32_t* __restrict__ ids, int P, int E, int cap,
     if (tid == 0 && bad && err != nullptr) atomicOr(err, 1);
 }
 
+// ---- the same permutation for many pairs, over several blocks --------------------------------------
+// Block b owns pairs [b*kPlanThreads, (b+1)*kPlanThreads). plan_hist_kernel counts each block's
+// pairs per expert; plan_base_kernel turns the counts into each (block, expert) first position -
+// the expert's offset plus the counts of the earlier blocks - and the offsets; plan_scatter_kernel
+// places each block's pairs in one round of the single-block kernel's stable scatter. Same result,
+// bit for bit: within an expert, pairs keep ascending pair order.
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+plan_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ blk,
+                 int32_t* __restrict__ err) {
+    extern __shared__ __align__(16) int smem_i[];
+    int* cnt = smem_i;                 // [E]
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += kPlanThreads) cnt[e] = 0;
+    __syncthreads();
+    const int p = blockIdx.x * kPlanThreads + tid;
+    bool bad = false;
+    if (p < P) {
+        const int e = ids[p];
+        if (e >= 0 && e < E)
+            atomicAdd(&cnt[e], 1);
+        else if (e != -1)
+            bad = true;
+    }
+    if (__syncthreads_or(bad) && tid == 0 && err != nullptr) atomicOr(err, 1);
+    for (int e = tid; e < E; e += kPlanThreads) blk[static_cast<size_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+plan_base_kernel(int P, int E, int nblk, int32_t* __restrict__ blk, int32_t* __restrict__ counts,
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair) {
+    extern __shared__ __align__(16) int smem_i[];
+    int* cnt = smem_i;                 // [E]
+    int* run = cnt + E;                // [E]
+    __shared__ int scratch[33];
+    const int tid = threadIdx.x;
+    // per expert: block bases relative to the expert, and its total
+    for (int e = tid; e < E; e += kPlanThreads) {
+        int acc = 0;
+        for (int b = 0; b < nblk; ++b) {
+            int32_t* q = blk + static_cast<size_t>(b) * E + e;
+            const int c = *q;
+            *q = acc;
+            acc += c;
+        }
+        cnt[e] = acc;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan(cnt, run, E, scratch);
+    for (int e = tid; e < E; e += kPlanThreads) {
+        counts[e] = cnt[e];
+        offsets[e] = run[e];
+        for (int b = 0; b < nblk; ++b) blk[static_cast<size_t>(b) * E + e] += run[e];
+    }
+    if (tid == 0) offsets[E] = total;
+    for (int s = total + tid; s < P; s += kPlanThreads) sorted_pair[s] = -1;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+plan_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* __restrict__ blk,
+                    int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_to_sorted) {
+    extern __shared__ __align__(16) int smem_i[];
+    uint8_t* pre = reinterpret_cast<uint8_t*>(smem_i);   // [32][E] per-warp counts
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < 32 * E; i += kPlanThreads) pre[i] = 0;
+    __syncthreads();
+    const int p = blockIdx.x * kPlanThreads + tid;
+    const int e = p < P ? ids[p] : -1;
+    const bool valid = p < P && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const int rank = __popc(peers & lanemask_lt());
+    if (valid && rank == 0) pre[warp * E + e] = static_cast<uint8_t>(__popc(peers));
+    __syncthreads();
+    if (valid) {
+        int s = 0;
+        for (int w = 0; w < warp; ++w) s += pre[w * E + e];
+        const int pos = blk[static_cast<size_t>(blockIdx.x) * E + e] + s + rank;
+        sorted_pair[pos] = p;
+        pair_to_sorted[p] = pos;
+    } else if (p < P) {
+        pair_to_sorted[p] = -1;
+    }
+}
+
+size_t route_plan_wide_ws_bytes(int P, int E) {
+    const size_t nblk = (static_cast<size_t>(P) + kPlanThreads - 1) / kPlanThreads;
+    return nblk * E * 4;
+}
+
+cudaError_t launch_route_plan_wide(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
+                                   int32_t* sorted_pair, int32_t* pair_to_sorted, int32_t* blk,
+                                   int32_t* err, cudaStream_t stream) {
+    const int nblk = (P + kPlanThreads - 1) / kPlanThreads;
+    const size_t s1 = static_cast<size_t>(E) * 4, s2 = static_cast<size_t>(E) * 8,
+                 s3 = static_cast<size_t>(E) * 32;
+    const void* fns[3] = {reinterpret_cast<const void*>(plan_hist_kernel),
+                          reinterpret_cast<const void*>(plan_base_kernel),
+                          reinterpret_cast<const void*>(plan_scatter_kernel)};
+    const size_t sm[3] = {s1, s2, s3};
+    for (int i = 0; i < 3; ++i)
+        if (sm[i] > 48 * 1024) {
+            cudaError_t st = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(sm[i]));
+            if (st != cudaSuccess) return st;
+        }
+    plan_hist_kernel<<<nblk, kPlanThreads, s1, stream>>>(ids, P, E, blk, err);
+    plan_base_kernel<<<1, kPlanThreads, s2, stream>>>(P, E, nblk, blk, counts, offsets, sorted_pair);
+    plan_scatter_kernel<<<nblk, kPlanThreads, s3, stream>>>(ids, P, E, blk, sorted_pair, pair_to_sorted);
+    return cudaGetLastError();
+}
+
 size_t route_plan_smem_bytes(int E) { return static_cast<size_t>(E) * (3 * 4 + 32); }
 
 cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,

@@ -324,3 +324,21 @@ def test_prefill_bitwise_repeatable():
     a = run(wl).clone()
     for _ in range(2):
         assert torch.equal(run(wl).view(torch.int16), a.view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_prefill_multi_block_plan(fmt):
+    """T*topk >= 4096 pairs: the permutation is planned over several blocks (a ragged last one),
+    with skew, a dropped slot (-1) and an out-of-range id; bit-for-bit the single-block result's
+    output, checked against the oracle."""
+    T, E = 700, 33
+    wl = inputs.make_custom(fmt, T, 256, 256, E, seed=960, device=DEV, routes="zipf")
+    ids = wl.ids.clone()
+    ids[:200, :3] = torch.tensor([0, 1, 2], dtype=torch.int32, device=DEV)
+    ids[9, 5] = -1
+    ids[650, 1] = E + 7
+    wl.ids = ids
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(wl, err=err)
+    assert int(err.item()) & capi.ERRBIT_BAD_ID
+    check_close(bf16_to_f64(out), oracle_for(wl)["out"], f"{fmt} prefill wide plan")

@@ -440,8 +440,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             for (int c0 = 0; c0 < 64 && c0 < vrows; c0 += 16) {
                 if (KIND == 0) {
                     float gv[16], uv[16];
-                    tmem_ld16(taddr + c0, gv);
-                    tmem_ld16(taddr + 128 + c0, uv);
+                    tmem_ld16x2(taddr + c0, taddr + 128 + c0, gv, uv);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int t = c0 + j;

@@ -17,6 +17,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -490,8 +491,10 @@ def bench_ours(args):
                                        for k, v in prefill_stage_ms.items()}},
                 "note": "f16 x f16 -> f32 MMA (same nominal rate as bf16); kernel times from the "
                         "library's stage events on the launching stream"}
-        # route plan, tile list, x prep, gate/up GEMM, activation prep, down GEMM, combine
-        launches_per_step = 7
+        # route plan (three launches from 4096 pairs on), tile list, x prep, gate/up GEMM,
+        # activation prep (only without a clamp limit <= 255), down GEMM, combine
+        launches_per_step = ((3 if P >= 4096 else 1) + 5
+                             + (0 if math.isfinite(inputs.LIMIT) and inputs.LIMIT <= 255 else 1))
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,

@@ -21,6 +21,8 @@
 // scale pre-multiplied by a power of two chosen per (expert, 128-row weight block) so the product
 // stays in f16's normal range (one f16 rounding per weight); the power of two is undone in the
 // fp32 epilogue. Products accumulate in fp32.
+#include <cmath>
+
 #include "prefill.cuh"
 #include "stage_timing.cuh"
 
@@ -396,6 +398,8 @@ __global__ void __launch_bounds__(prefill::kThreads, 2) prefill_gemm_kernel(cons
 
 // pairs from which the prefill tier plans its permutation over several blocks
 constexpr int kWidePlanPairs = 4096;
+// largest clamp limit L for which a (|a| <= L^2) is stored in f16 without a range scale
+constexpr float kA16DirectLimit = 255.0f;
 
 PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     const size_t P = static_cast<size_t>(T) * topk;
@@ -465,7 +469,11 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
                                                   MOE_PREFILL_TC >= 3 ? I32(L.pair_to_sorted) : nullptr, topk);
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
-    if ((st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess) return st;
+    // a finite clamp limit L <= 255 bounds |a| = |silu(min(g, L)) * clamp(u, -L, L)| by L^2, which
+    // f16 holds without a range scale: the TMEM core then writes a in f16 itself
+    const bool a16_direct = MOE_PREFILL_TC == 4 && std::isfinite(limit) && limit <= kA16DirectLimit;
+    if (!a16_direct && (st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess)
+        return st;
 
     const int grid = gemm_grid();
     if (grid <= 0) return cudaErrorInvalidDevice;
@@ -497,6 +505,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     gu.limit = limit;
     gu.out = f32;
     gu.amax = amax;
+    gu.out16 = a16_direct ? reinterpret_cast<__half*>(ws + L.a16) : nullptr;
     gu.out_ld = I;
     gu.err = err;
     gu.a_rows = MOE_PREFILL_TC >= 3 ? P : T;
@@ -522,15 +531,18 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
 
     __half* a16 = reinterpret_cast<__half*>(ws + L.a16);
     float* ainv = reinterpret_cast<float*>(ws + L.ainv);
-    stage_mark(stream, "act_prep");
-    prefill_act_prep_kernel<<<P, 256, 0, stream>>>(f32, amax, I32(L.offsets) + E, I, a16, ainv);
-    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    if (!a16_direct) {
+        stage_mark(stream, "act_prep");
+        prefill_act_prep_kernel<<<P, 256, 0, stream>>>(f32, amax, I32(L.offsets) + E, I, a16, ainv);
+        if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    }
 
     PrefillGemmArgs dn = gu;
     dn.K = I;
     dn.n_tiles = H / prefill::kBN;
     dn.a = a16;
-    dn.a_inv = ainv;
+    dn.a_inv = a16_direct ? nullptr : ainv;
+    dn.out16 = nullptr;
     dn.w0 = wd;
     dn.s0 = sd;
     dn.w1 = wd;

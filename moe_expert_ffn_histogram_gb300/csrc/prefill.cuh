@@ -43,6 +43,10 @@ struct PrefillGemmArgs {
     // outputs
     float* out;                  // KIND 0: a32 [P][I]; KIND 1: y [P][H]
     uint32_t* amax;              // KIND 0: per sorted row max |a| (float bits), zeroed before
+    // KIND 0, TMEM core: when set, a goes straight to f16 here ([P][I], no range scale: a finite
+    // clamp limit L <= 255 bounds |a| by L^2 < 65504), and out / amax are not used; KIND 1 then
+    // runs with a_inv == nullptr (scale 1)
+    __half* out16;
     int out_ld;                  // I (KIND 0) or H (KIND 1)
     int32_t* err;                // optional error word (bit 1: a bounded wait gave up)
     int a_rows;                  // rows of the A matrix: T (KIND 0) or P (KIND 1)

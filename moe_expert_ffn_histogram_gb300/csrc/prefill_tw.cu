@@ -415,7 +415,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int rr = r0 + min(cbase + 32 * i + lane, rows - 1);
-                xs_s[ew][32 * i + lane] = KIND == 0 ? p.a_inv[p.sorted_pair[rr] / p.topk] : p.a_inv[rr];
+                xs_s[ew][32 * i + lane] = KIND == 0       ? p.a_inv[p.sorted_pair[rr] / p.topk]
+                                          : p.a_inv != nullptr ? p.a_inv[rr]
+                                                               : 1.0f;
             }
             const size_t sblk = static_cast<size_t>(e) * (p.wrows / 128) + nt;
             float winv0, winv1;                            // undo the converters' weight scaling
@@ -435,6 +437,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem + lane_off + b * Cfg::kAccCols + cbase;
             float* dst = p.out + static_cast<size_t>(r0 + cbase) * p.out_ld + nt * 128 + f;
+            __half* dst16 = KIND == 0 && p.out16 != nullptr
+                                ? p.out16 + static_cast<size_t>(r0 + cbase) * p.out_ld + nt * 128 + f
+                                : nullptr;
             const int vrows = rows - cbase;                // valid columns of this warp
 #pragma unroll 1
             for (int c0 = 0; c0 < 64 && c0 < vrows; c0 += 16) {
@@ -450,10 +455,14 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                         const float gg = fminf(gv[j] * xs * winv0, p.limit);
                         const float uu = fminf(fmaxf(uv[j] * xs * winv1, -p.limit), p.limit);
                         const float h = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
-                        const uint32_t mb = warp_max_bits(fabsf(h));
-                        if (t < vrows) {
-                            dst[static_cast<size_t>(t) * p.out_ld] = h;
-                            if (lane == 0) atomicMax(p.amax + r0 + cbase + t, mb);
+                        if (dst16 != nullptr) {                // bounded by the clamp: f16 as is
+                            if (t < vrows) dst16[static_cast<size_t>(t) * p.out_ld] = __float2half_rn(h);
+                        } else {
+                            const uint32_t mb = warp_max_bits(fabsf(h));
+                            if (t < vrows) {
+                                dst[static_cast<size_t>(t) * p.out_ld] = h;
+                                if (lane == 0) atomicMax(p.amax + r0 + cbase + t, mb);
+                            }
                         }
                     }
                 } else {

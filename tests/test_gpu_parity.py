@@ -342,3 +342,12 @@ def test_prefill_multi_block_plan(fmt):
     out = run(wl, err=err)
     assert int(err.item()) & capi.ERRBIT_BAD_ID
     check_close(bf16_to_f64(out), oracle_for(wl)["out"], f"{fmt} prefill wide plan")
+
+
+@pytest.mark.parametrize("limit", [255.0, 300.0])
+def test_prefill_activation_paths_at_the_limit_bound(limit):
+    """limit <= 255: the gate/up GEMM stores the activations in f16 as they are (|a| <= limit^2
+    fits f16); above it they keep the per-row range scale (act_prep). Both against the oracle
+    with large activations."""
+    wl = inputs.make_custom("fp8", 48, 256, 256, 10, seed=966, device=DEV, x_scale=60.0, limit=limit)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"prefill limit {limit}")

@@ -26,7 +26,8 @@ def _timed(wl):
 @pytest.mark.parametrize("T,names", [
     (1, ["plan", "gate_up", "down_combine"]),
     (5, ["fused"]),
-    (64, ["route_plan", "tile_list", "x_prep", "gate_up_gemm", "act_prep", "down_gemm", "combine"]),
+    # a finite clamp limit bounds the activations: the gate/up GEMM writes them in f16 itself
+    (64, ["route_plan", "tile_list", "x_prep", "gate_up_gemm", "down_gemm", "combine"]),
 ])
 def test_stage_names_and_times(T, names):
     wl = inputs.make_custom("fp8", T, 512, 256, 16, seed=900 + T, device=DEV)
@@ -35,6 +36,15 @@ def test_stage_names_and_times(T, names):
     assert [n for n, _ in st] == names
     assert all(ms >= 0.0 for _, ms in st)
     assert sum(ms for _, ms in st) <= total * 1.05 + 0.05
+
+
+def test_stage_names_without_clamp():
+    """No clamp (limit = +inf): the activations need their range scale, so act_prep runs."""
+    wl = inputs.make_custom("fp8", 64, 512, 256, 16, seed=964, device=DEV, limit=float("inf"))
+    capi.forward(wl.x, wl.ids, wl.wts, wl.bank, wl.limit)
+    st, _ = _timed(wl)
+    assert [n for n, _ in st] == ["route_plan", "tile_list", "x_prep", "gate_up_gemm", "act_prep",
+                                  "down_gemm", "combine"]
 
 
 def test_timing_off_records_nothing():

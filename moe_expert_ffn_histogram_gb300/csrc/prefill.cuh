@@ -88,6 +88,21 @@ __device__ __forceinline__ float weight_prescale(const float* srow, int KB, uint
     return inv;
 }
 
+// The same table from scales already in registers: lane holds kb = lane (v0) and lane + 32 (v1),
+// zero past KB (KB <= 64). One warp.
+__device__ __forceinline__ void prescale_from_regs(float v0, float v1, int KB, uint32_t* tbl) {
+    const int lane = threadIdx.x & 31;
+    const float m = warp_max(fmaxf(fabsf(v0), fabsf(v1))) * 448.0f;
+    float inv;
+    const float pre = pow2_range_scale(m, inv);
+    auto splat = [&](float v) {
+        const __half h = __float2half_rn(v * pre);
+        return static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&h)) * 0x10001u;
+    };
+    if (lane < KB) tbl[lane] = splat(v0);
+    if (lane + 32 < KB) tbl[lane + 32] = splat(v1);
+}
+
 // Launch one grouped GEMM (KIND 0: gate/up + SwiGLU, KIND 1: down) on the simple tcgen05 core
 // (prefill_tc.cu) or the warp-specialised one (prefill_ws.cu; N_total = I or H, it picks its own
 // column tiling and sets n_tiles).

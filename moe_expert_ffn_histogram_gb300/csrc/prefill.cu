@@ -7,17 +7,18 @@
 // projection, with `moe_sort_by_expert` before it and the `_indexed` combine after it (same slot
 // order and rounding as the narrow tiers). Here:
 //
-//   route_plan (existing)    counts / offsets / sorted_pair / pair_to_sorted
+//   route plan               counts / offsets / sorted_pair / pair_to_sorted (route_plan.cu)
 //   prefill_tiles            the m-tile list: (expert, first sorted row) per 128-row tile
-//   prefill_x_prep           x (bf16) -> x16 (f16, one power-of-two range scale per token)
-//   prefill_gateup_gemm      per tile of 128 sorted rows x 64 features: gate and up from the
-//                            same weight tile walk, clamped SwiGLU in the epilogue -> a (fp32) and
-//                            a per-row running max |a|
-//   prefill_act_prep         a (fp32) -> a16 (f16, one power-of-two range scale per sorted row)
-//   prefill_down_gemm        per tile of 128 sorted rows x 128 output columns: y (fp32)
+//   prefill_x_prep           x (bf16) -> x16 (f16, one power-of-two range scale per token), each
+//                            token's row written to its routed pairs' sorted rows
+//   gate/up grouped GEMM     per tile of 128 sorted rows x 128 features: gate and up, clamped
+//                            SwiGLU in the epilogue -> a (prefill_tw.cu, the TMEM core)
+//   prefill_act_prep         a (fp32) -> a16 (f16, one power-of-two range scale per sorted row),
+//                            only when no clamp limit bounds a (with one the GEMM writes a16)
+//   down grouped GEMM        per tile of 128 sorted rows x 128 output rows: y (fp32)
 //   prefill_combine          out[t] = sum over slots k in order of w[t,k] * y[pair_to_sorted], bf16
 //
-// Weights are dequantised while building MMA fragments: E4M3 -> f16 exactly, times the block
+// Weights are dequantised by the GEMM's converter warps: E4M3 -> f16 exactly, times the block
 // scale pre-multiplied by a power of two chosen per (expert, 128-row weight block) so the product
 // stays in f16's normal range (one f16 rounding per weight); the power of two is undone in the
 // fp32 epilogue. Products accumulate in fp32.
@@ -25,13 +26,6 @@
 
 #include "prefill.cuh"
 #include "stage_timing.cuh"
-
-// Which grouped-GEMM core the prefill tier launches: 4 = weights in TMEM (prefill_tw.cu),
-// 3 = TMA-fed warp-specialised tcgen05/TMEM (prefill_tma.cu), 2 = cp.async-fed warp-specialised (prefill_ws.cu), 1 = simple tcgen05/TMEM
-// (prefill_tc.cu), 0 = mma.sync (below).
-#ifndef MOE_PREFILL_TC
-#define MOE_PREFILL_TC 4
-#endif
 
 namespace moe {
 
@@ -210,190 +204,6 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
     }
 }
 
-// ---- grouped GEMMs (mma.sync m16n8k16 f16 -> f32) ------------------------------------------------
-
-
-template <int KIND>
-__global__ void __launch_bounds__(prefill::kThreads, 2) prefill_gemm_kernel(const PrefillGemmArgs p) {
-    using namespace prefill;
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t* sa = smem;                               // [kStages][kBM][kARow]
-    uint8_t* sb = smem + kStages * kAStage;           // [kStages][kBN][kBRow]
-    __shared__ const __half* a_row[kBM];              // A row sources of this tile
-    __shared__ float a_scale[kBM];                    // their inverse range scales
-    __shared__ uint32_t w_scale[2][64];               // per 128-wide K block: f16x2 splat of the
-                                                      // prescaled block scale (gate/down, up)
-    __shared__ float w_inv[2];                        // the inverse of the power-of-two prescale
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, c = lane & 3;
-    const int wm = warp >> 2, wn = warp & 3;
-    const int K = p.K, KT = K / kBK, KB = K / 128;
-    const int total = p.tiles[0] * p.n_tiles;
-
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
-        const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
-        const int rows = min(kBM, p.offsets[e + 1] - r0);
-
-        // ---- per-tile tables: A row sources and scales, weight block scales ----
-        __syncthreads();                              // previous tile's readers are done
-        if (tid < kBM) {
-            const int r = r0 + min(tid, rows - 1);    // padded rows repeat the last valid row
-            if (KIND == 0) {
-                const int t = p.sorted_pair[r] / p.topk;
-                a_row[tid] = p.a + static_cast<size_t>(t) * K;
-                a_scale[tid] = p.a_inv[t];
-            } else {
-                a_row[tid] = p.a + static_cast<size_t>(r) * K;
-                a_scale[tid] = p.a_inv[r];
-            }
-        }
-        if (warp < 2) {                               // warp 0: gate/down scales, warp 1: up
-            const int nb = KIND == 0 ? (nt * 64) / 128 : nt;
-            const float* srow = (warp == 0 ? p.s0 : p.s1) + (static_cast<size_t>(e) * (p.wrows / 128) + nb) * KB;
-            if (KIND == 1 && warp == 1) srow = p.s0 + (static_cast<size_t>(e) * (p.wrows / 128) + nb) * KB;
-            float m = 0.0f;
-            for (int kb = lane; kb < KB; kb += 32) m = fmaxf(m, fabsf(srow[kb]));
-            m = warp_max(m) * 448.0f;
-            float inv;
-            const float pre = pow2_range_scale(m, inv);
-            for (int kb = lane; kb < KB; kb += 32) {
-                const __half h = __float2half_rn(srow[kb] * pre);
-                const uint16_t hb = *reinterpret_cast<const uint16_t*>(&h);
-                w_scale[warp][kb] = static_cast<uint32_t>(hb) * 0x10001u;
-            }
-            if (lane == 0) w_inv[warp] = inv;
-        }
-        __syncthreads();
-
-        // ---- loader: stage s <- K slice kt ----
-        auto load = [&](int kt, int s) {
-            uint8_t* dA = sa + s * kAStage;
-            uint8_t* dB = sb + s * kBStage;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {             // A: 128 rows x 8 chunks of 16 B
-                const int ch = tid + i * kThreads, r = ch >> 3, q = ch & 7;
-                cp_async16(dA + r * kARow + q * 16, a_row[r] + kt * kBK + q * 8);
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {             // B: 128 weight rows x 4 chunks of 16 B
-                const int ch = tid + i * kThreads, n = ch >> 2, q = ch & 3;
-                const uint8_t* src;
-                if (KIND == 0) {
-                    // tile row n -> warp column group j, fragment f, row gg: fragments 0,1 are gate
-                    // rows and 2,3 the matching up rows of the same 16 features
-                    const int j = n >> 5, f = (n & 31) >> 3, gg = n & 7;
-                    const int feat = nt * 64 + 16 * j + 8 * (f & 1) + gg;
-                    src = (f < 2 ? p.w0 : p.w1) + (static_cast<size_t>(e) * p.wrows + feat) * K;
-                } else {
-                    src = p.w0 + (static_cast<size_t>(e) * p.wrows + nt * kBN + n) * K;
-                }
-                cp_async16(dB + n * kBRow + q * 16, src + kt * kBK + q * 16);
-            }
-        };
-
-        float acc[4][4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int f = 0; f < 4; ++f)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[i][f][r] = 0.0f;
-
-        load(0, 0);
-        cp_async_commit();
-        if (KT > 1) load(1, 1);
-        cp_async_commit();
-        for (int kt = 0; kt < KT; ++kt) {
-            cp_async_wait<1>();
-            __syncthreads();
-            if (kt + 2 < KT) load(kt + 2, (kt + 2) % kStages);
-            cp_async_commit();
-            const uint8_t* A = sa + (kt % kStages) * kAStage;
-            const uint8_t* B = sb + (kt % kStages) * kBStage;
-            const uint32_t sc0 = w_scale[0][(kt * kBK) / 128];
-            const uint32_t sc1 = KIND == 0 ? w_scale[1][(kt * kBK) / 128] : sc0;
-#pragma unroll
-            for (int q = 0; q < kBK / 16; ++q) {
-                uint32_t af[4][4], bf[4][2];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = wm * 64 + 16 * i + g;
-                    const uint2 lo = lds64(A + row * kARow + (q * 16 + 4 * c) * 2);
-                    const uint2 hi = lds64(A + (row + 8) * kARow + (q * 16 + 4 * c) * 2);
-                    af[i][0] = lo.x;
-                    af[i][1] = hi.x;
-                    af[i][2] = lo.y;
-                    af[i][3] = hi.y;
-                }
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const int n = wn * 32 + 8 * f + g;
-                    const uint32_t w4 = *reinterpret_cast<const uint32_t*>(B + n * kBRow + q * 16 + 4 * c);
-                    uint32_t lo, hi;
-                    e4m3x4_to_f16x2x2(w4, lo, hi);
-                    const uint32_t sc = (KIND == 0 && f >= 2) ? sc1 : sc0;
-                    bf[f][0] = hmul2(lo, sc);
-                    bf[f][1] = hmul2(hi, sc);
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int f = 0; f < 4; ++f)
-                        mma_f16(acc[i][f], af[i][0], af[i][1], af[i][2], af[i][3], bf[f][0], bf[f][1]);
-            }
-        }
-        cp_async_wait<0>();
-
-        // ---- epilogue ----
-        if (KIND == 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                for (int hrow = 0; hrow < 2; ++hrow) {
-                    const int row = wm * 64 + 16 * i + g + 8 * hrow;
-                    const float xs = a_scale[row];
-                    float m = 0.0f;
-                    float hv[2][2];
-#pragma unroll
-                    for (int f = 0; f < 2; ++f)
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const float gv = acc[i][f][2 * hrow + j] * xs * w_inv[0];
-                            const float uv = acc[i][f + 2][2 * hrow + j] * xs * w_inv[1];
-                            hv[f][j] = clamped_swiglu(gv, uv, p.limit);
-                            m = fmaxf(m, fabsf(hv[f][j]));
-                        }
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    if (row < rows) {
-                        float* dst = p.out + static_cast<size_t>(r0 + row) * p.out_ld + nt * 64 + 16 * wn;
-#pragma unroll
-                        for (int f = 0; f < 2; ++f)
-                            *reinterpret_cast<float2*>(dst + 8 * f + 2 * c) = make_float2(hv[f][0], hv[f][1]);
-                        if (c == 0) atomicMax(p.amax + r0 + row, __float_as_uint(m));
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                for (int hrow = 0; hrow < 2; ++hrow) {
-                    const int row = wm * 64 + 16 * i + g + 8 * hrow;
-                    if (row >= rows) continue;
-                    const float sc = a_scale[row] * w_inv[0];
-                    float* dst = p.out + static_cast<size_t>(r0 + row) * p.out_ld + nt * kBN + wn * 32;
-#pragma unroll
-                    for (int f = 0; f < 4; ++f)
-                        *reinterpret_cast<float2*>(dst + 8 * f + 2 * c) =
-                            make_float2(acc[i][f][2 * hrow] * sc, acc[i][f][2 * hrow + 1] * sc);
-                }
-            }
-        }
-    }
-}
-
 // ---- workspace and launch sequence ------------------------------------------------------------------
 
 // pairs from which the prefill tier plans its permutation over several blocks
@@ -416,7 +226,7 @@ PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     L.tile_r0 = take(mtiles * 4);
     L.tile_first = take(mtiles * 4);
     L.tile_cnt = take(mtiles * 4);
-    L.x16 = take((MOE_PREFILL_TC >= 3 ? P : static_cast<size_t>(T)) * H * 2);   // [P][H] sorted for TMA
+    L.x16 = take(P * H * 2);                       // [P][H], in sorted-row order for the TMA boxes
     L.xinv = take(static_cast<size_t>(T) * 4);
     L.amax = take(P * 4);
     L.a16 = take(P * static_cast<size_t>(I) * 2);
@@ -427,22 +237,11 @@ PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     return L;
 }
 
-namespace {
-
-int gemm_grid() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return 2 * sms;
-}
-
-}  // namespace
 
 cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
                            const int32_t* ids, const float* wts, const PrefillWeights& wt, float limit,
                            __nv_bfloat16* out, uint8_t* ws, const PrefillLayout& L, int32_t* err,
                            cudaStream_t stream, const __nv_bfloat16* shared, const __nv_bfloat16* residual) {
-    if (fmt == 1 && MOE_PREFILL_TC != 4) return cudaErrorNotSupported;   // NVFP4: TMEM core only
     const uint8_t *wg = wt.wg, *wu = wt.wu, *wd = wt.wd;
     const float *sg = wt.sg, *su = wt.su, *sd = wt.sd;
     const int P = T * topk;
@@ -466,23 +265,15 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     float* xinv = reinterpret_cast<float*>(ws + L.xinv);
     stage_mark(stream, "x_prep");
     prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv,
-                                                  MOE_PREFILL_TC >= 3 ? I32(L.pair_to_sorted) : nullptr, topk);
+                                                  I32(L.pair_to_sorted), topk);
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
     // a finite clamp limit L <= 255 bounds |a| = |silu(min(g, L)) * clamp(u, -L, L)| by L^2, which
     // f16 holds without a range scale: the TMEM core then writes a in f16 itself
-    const bool a16_direct = MOE_PREFILL_TC == 4 && std::isfinite(limit) && limit <= kA16DirectLimit;
+    const bool a16_direct = std::isfinite(limit) && limit <= kA16DirectLimit;
     if (!a16_direct && (st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess)
         return st;
 
-    const int grid = gemm_grid();
-    if (grid <= 0) return cudaErrorInvalidDevice;
-    if ((st = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   prefill::kSmem)) != cudaSuccess)
-        return st;
-    if ((st = cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   prefill::kSmem)) != cudaSuccess)
-        return st;
     float* f32 = reinterpret_cast<float*>(ws + L.f32);
     PrefillGemmArgs gu{};
     gu.tiles = I32(L.tiles);
@@ -508,7 +299,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     gu.out16 = a16_direct ? reinterpret_cast<__half*>(ws + L.a16) : nullptr;
     gu.out_ld = I;
     gu.err = err;
-    gu.a_rows = MOE_PREFILL_TC >= 3 ? P : T;
+    gu.a_rows = P;
     gu.experts = E;
     gu.fmt = fmt;
     gu.sf0 = wt.sfg;
@@ -516,18 +307,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     gu.s2_0 = wt.s2g;
     gu.s2_1 = wt.s2u;
     stage_mark(stream, "gate_up_gemm");
-    if (MOE_PREFILL_TC == 4) {
-        if ((st = launch_prefill_gemm_tw(0, gu, I, stream)) != cudaSuccess) return st;
-    } else if (MOE_PREFILL_TC == 3) {
-        if ((st = launch_prefill_gemm_tma(0, gu, I, stream)) != cudaSuccess) return st;
-    } else if (MOE_PREFILL_TC == 2) {
-        if ((st = launch_prefill_gemm_ws(0, gu, I, stream)) != cudaSuccess) return st;
-    } else if (MOE_PREFILL_TC == 1) {
-        if ((st = launch_prefill_gemm_tc(0, gu, stream)) != cudaSuccess) return st;
-    } else {
-        prefill_gemm_kernel<0><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(gu);
-        if ((st = cudaGetLastError()) != cudaSuccess) return st;
-    }
+    if ((st = launch_prefill_gemm_tw(0, gu, I, stream)) != cudaSuccess) return st;
 
     __half* a16 = reinterpret_cast<__half*>(ws + L.a16);
     float* ainv = reinterpret_cast<float*>(ws + L.ainv);
@@ -557,18 +337,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     dn.out_ld = H;
     dn.a_rows = P;
     stage_mark(stream, "down_gemm");
-    if (MOE_PREFILL_TC == 4) {
-        if ((st = launch_prefill_gemm_tw(1, dn, H, stream)) != cudaSuccess) return st;
-    } else if (MOE_PREFILL_TC == 3) {
-        if ((st = launch_prefill_gemm_tma(1, dn, H, stream)) != cudaSuccess) return st;
-    } else if (MOE_PREFILL_TC == 2) {
-        if ((st = launch_prefill_gemm_ws(1, dn, H, stream)) != cudaSuccess) return st;
-    } else if (MOE_PREFILL_TC == 1) {
-        if ((st = launch_prefill_gemm_tc(1, dn, stream)) != cudaSuccess) return st;
-    } else {
-        prefill_gemm_kernel<1><<<grid, prefill::kThreads, prefill::kSmem, stream>>>(dn);
-        if ((st = cudaGetLastError()) != cudaSuccess) return st;
-    }
+    if ((st = launch_prefill_gemm_tw(1, dn, H, stream)) != cudaSuccess) return st;
 
     stage_mark(stream, "combine");
     prefill_combine_kernel<<<T, 256, 0, stream>>>(f32, I32(L.pair_to_sorted), wts, topk, H, out, shared,

@@ -1,5 +1,5 @@
-// Shared pieces of the grouped-GEMM (prefill) tier: tile shape, the GEMM argument block, and
-// the two GEMM cores (mma.sync in prefill.cu, tcgen05/TMEM in prefill_tc.cu).
+// Shared pieces of the grouped-GEMM (prefill) tier: tile shape, the GEMM argument block and the
+// per-tile helpers of the tensor-memory GEMM core (prefill_tw.cu).
 #pragma once
 #include "gemv_items.cuh"
 
@@ -8,15 +8,7 @@ namespace moe {
 namespace prefill {
 
 constexpr int kBM = 128;               // sorted rows per tile
-constexpr int kBN = 128;               // weight rows per tile (gate/up: 64 gate + the same 64 up)
-constexpr int kBK = 64;                // K per pipeline stage
-constexpr int kThreads = 256;          // 8 warps: 2 (rows) x 4 (columns), warp tile 64 x 32
-constexpr int kStages = 3;
-constexpr int kARow = kBK * 2 + 32;    // A smem row pitch in bytes (f16 + 32 B pad: no conflicts)
-constexpr int kBRow = kBK + 16;        // B smem row pitch in bytes (fp8 + 16 B pad: no conflicts)
-constexpr int kAStage = kBM * kARow;
-constexpr int kBStage = kBN * kBRow;
-constexpr int kSmem = kStages * (kAStage + kBStage);
+constexpr int kBN = 128;               // weight rows per tile (gate/up: 128 gate + the same 128 up)
 
 }  // namespace prefill
 
@@ -30,7 +22,7 @@ struct PrefillGemmArgs {
     const int32_t* offsets;      // [E+1]
     const int32_t* sorted_pair;  // [P]
     int topk, K, n_tiles;
-    // A operand: rows of a16 (KIND 1) or rows of x16 gathered through sorted_pair (KIND 0)
+    // A operand: sorted rows of x16 (KIND 0) or of a16 (KIND 1), f16
     const __half* a;
     const float* a_inv;          // per token (KIND 0) or per sorted row (KIND 1)
     // B operand: E4M3 weight rows and fp32 block scales; KIND 0 uses both gate (w0) and up (w1)
@@ -103,14 +95,7 @@ __device__ __forceinline__ void prescale_from_regs(float v0, float v1, int KB, u
     if (lane + 32 < KB) tbl[lane + 32] = splat(v1);
 }
 
-// Launch one grouped GEMM (KIND 0: gate/up + SwiGLU, KIND 1: down) on the simple tcgen05 core
-// (prefill_tc.cu) or the warp-specialised one (prefill_ws.cu; N_total = I or H, it picks its own
-// column tiling and sets n_tiles).
-cudaError_t launch_prefill_gemm_tc(int kind, const PrefillGemmArgs& p, cudaStream_t stream);
-cudaError_t launch_prefill_gemm_ws(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
-// TMA-fed variant of the warp-specialised core (prefill_tma.cu): A and the E4M3 weight slices
-// arrive by tensor-map copies (a row gather for the gate/up activations).
-cudaError_t launch_prefill_gemm_tma(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);
+
 // Transposed variant with the dequantised weights as the MMA's TMEM operand (prefill_tw.cu);
 // FP8 or NVFP4 weights (p.fmt).
 cudaError_t launch_prefill_gemm_tw(int kind, const PrefillGemmArgs& p, int N_total, cudaStream_t stream);

@@ -5,7 +5,7 @@
 // (TMA, 128-byte swizzled) as its B operand in shared memory. Dequantised weights thus never
 // pass through shared memory: per 128-wide K slice shared memory carries the token boxes, the
 // raw weight boxes and their one read by the converters - the f16 round trip through shared
-// memory is what bounded the core that staged the dequantised weights there (prefill_tma.cu).
+// memory is what bounded an earlier core that staged the dequantised weights there.
 //   warps 0-1    token producers  slice sc -> token slot sc % NT (two TMA boxes of 128 rows x 64
 //                                 f16), once the slot's previous MMAs are done;
 //   warps 2-3    raw producers    slice sc -> raw stage sc % NR (per weight matrix one box of 128

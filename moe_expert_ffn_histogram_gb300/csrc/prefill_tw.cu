@@ -40,15 +40,6 @@
 #include "prefill.cuh"
 #include "tc_ptx.cuh"
 
-#ifndef MOE_TW_CE_GU
-#define MOE_TW_CE_GU 1
-#endif
-#ifndef MOE_TW_CE_DN
-#define MOE_TW_CE_DN 1
-#endif
-#ifndef MOE_TW_EPI_SPIN
-#define MOE_TW_EPI_SPIN 0
-#endif
 
 namespace moe {
 
@@ -93,7 +84,6 @@ struct TwCfg {
     // raw stages: as many as fit beside the token slots (at least 120 KB in all, so that one CTA
     // - and one 512-column TMEM allocation - fits per SM)
     static constexpr int kRawStages = (NM == 2 && FMT == 0) ? 3 : (NM == 1 && FMT == 0) ? 5 : (NM == 2) ? 5 : 6;
-    static constexpr int kCommitSlices = NM == 2 ? MOE_TW_CE_GU : MOE_TW_CE_DN;
     static constexpr int kSmemUsed = kTokSlots * kTwTok + kRawStages * kRaw + 1024;
     static constexpr int kSmem = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
     static constexpr int kAcc = DB ? 2 : 1;                // accumulator buffers
@@ -103,7 +93,6 @@ struct TwCfg {
     static constexpr uint32_t kA0 = kAcc * kAccCols;       // first A column
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kA0 + kSlots * kACols <= kTmemCols && kSlots <= kTwSlotsMax && kTokSlots <= kTwSlotsMax, "TMEM budget");
-    static_assert(kSlots % kCommitSlices == 0, "slot groups");
     static_assert(kSmemUsed + 6 * 1024 <= 227 * 1024, "shared memory");
     static_assert(kRaw % 1024 == 0 && kTwTok % 1024 == 0, "stage alignment");
 };
@@ -115,14 +104,14 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     prefill_tw_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ CUtensorMap tmTok,
                            const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1) {
     using Cfg = TwCfg<NM, DB, FMT>;
-    constexpr int NS = Cfg::kSlots, NT = Cfg::kTokSlots, NR = Cfg::kRawStages, CE = Cfg::kCommitSlices;
+    constexpr int NS = Cfg::kSlots, NT = Cfg::kTokSlots, NR = Cfg::kRawStages;
     constexpr uint32_t kIdesc128 = idesc_f16_f32<128, 128>();
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     // tfull[t]: token boxes of token slot t landed; tempty[t]: its MMAs are done (own token
     // slots only); rfull/rempty[r]: raw boxes r landed / read by all converters; afull[s]: weight
-    // slice s in TMEM; sempty[g]: the MMAs of slot group g (slots g*CE..+CE-1: their TMEM slices,
-    // and their token boxes when those are not on their own) are done; acc_full/acc_empty[b]:
+    // slice s in TMEM; sempty[s]: the MMAs of slot s are done (its TMEM slice - and its token
+    // boxes when those are not on their own - may be refilled); acc_full/acc_empty[b]:
     // accumulator b complete / drained.
     __shared__ __align__(8) uint64_t tfull[NT], tempty[NT], afull[NS], sempty[NS], rfull[NR], rempty[NR], acc_full[2],
         acc_empty[2];
@@ -143,7 +132,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
         }
         for (int s = 0; s < NS; ++s) {
             mbar_init(&afull[s], kTwConvWarps);
-            if (s < NS / CE) mbar_init(&sempty[s], 1);
+            mbar_init(&sempty[s], 1);
         }
         for (int r = 0; r < NR; ++r) {
             mbar_init(&rfull[r], 1);
@@ -184,7 +173,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                     if (static_cast<int>(sc % 2) != pw) continue;
                     if (tok) {
                         const uint32_t s = sc % NT, u = sc / NT;
-                        if (u > 0 && !tw_wait(Cfg::kTokOwn ? &tempty[s] : &sempty[s / CE], (u - 1) & 1u)) {
+                        if (u > 0 && !tw_wait(Cfg::kTokOwn ? &tempty[s] : &sempty[s], (u - 1) & 1u)) {
                             ok = false;
                             break;
                         }
@@ -340,7 +329,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                             }
                         }
                     }
-                    if (pc == 0 && !__all_sync(0xffffffffu, us == 0 || tw_wait(&sempty[s / CE], (us - 1) & 1u))) {
+                    if (pc == 0 && !__all_sync(0xffffffffu, us == 0 || tw_wait(&sempty[s], (us - 1) & 1u))) {
                         ok = false;
                         break;
                     }
@@ -399,7 +388,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                             mma_issue_tmem_a(d0 + m * 128, a0 + m * Cfg::kMCols + kk * 8, bdesc, idesc,
                                              (kt > 0 || kk > 0) ? 1u : 0u);
                     }
-                    if (s % CE == CE - 1) mma_commit(&sempty[s / CE]);
+                    mma_commit(&sempty[s]);
                     if (Cfg::kTokOwn) mma_commit(&tempty[t]);
                     if (kt == KT - 1) mma_commit(&acc_full[b]);
                 }
@@ -480,7 +469,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             }
             __syncwarp();
             const uint32_t b = tcount % Cfg::kAcc, v = tcount / Cfg::kAcc;
-            if (!__all_sync(0xffffffffu, MOE_TW_EPI_SPIN ? tw_wait(&acc_full[b], v & 1u) : mbar_wait_sleep(&acc_full[b], v & 1u))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(&acc_full[b], v & 1u))) {
                 abort_s = 1;
                 break;
             }

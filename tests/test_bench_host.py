@@ -1,0 +1,71 @@
+"""Host logic of bench.py (no GPU): the algorithmic byte counts behind the roofline, and the rule
+that a committed DRAM-traffic figure is reported only while the kernel's sources are unchanged."""
+import json
+import os
+import sys
+import types
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _wl(fmt, T, H, I, E, ids):
+    return types.SimpleNamespace(fmt=fmt, T=T, H=H, I=I, E=E, topk=8, ids=torch.tensor(ids, dtype=torch.int32))
+
+
+def test_matrix_bytes_fp8_and_nvfp4():
+    # FP8: one byte per code + one fp32 per 128x128 block; NVFP4: half a byte per code + one byte per 16
+    assert bench.matrix_bytes("fp8", 2048, 7168) == 2048 * 7168 + 16 * 56 * 4
+    assert bench.matrix_bytes("nvfp4", 1536, 5120) == 1536 * 5120 // 2 + 1536 * 320
+
+
+def test_alg_bytes_counts_each_distinct_expert_once():
+    H, I = 7168, 2048
+    # two tokens sharing expert 3; -1 and an out-of-range id add nothing
+    ids = [[3, 1, 2, 4, 5, 6, 7, 8], [3, 9, 10, 11, 12, -1, 99, 13]]
+    b = bench.alg_bytes(_wl("fp8", 2, H, I, 16, ids))
+    distinct = 13   # {1..13} minus nothing: 3 counted once, -1 and 99 dropped
+    assert b["distinct"] == distinct
+    w = distinct * (2 * bench.matrix_bytes("fp8", I, H) + bench.matrix_bytes("fp8", H, I))
+    assert b["weights"] == w
+    assert b["total"] == w + 2 * H * 2 + 2 * H * 2 + 16 * 8
+    # the single-token decode figure quoted in the docs: 8 experts x 3 x 7168 x 2048 codes + scales
+    one = bench.alg_bytes(_wl("fp8", 1, H, I, 256, [list(range(8))]))
+    assert one["weights"] == 8 * 3 * (H * I + 16 * 56 * 4)
+
+
+def test_profiled_traffic_only_for_unchanged_sources(tmp_path, monkeypatch):
+    csrc = tmp_path / "moe_expert_ffn_histogram_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1")
+    (csrc / "h.cuh").write_text("header v1")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.kernel_source_sha(["k.cu", "h.cuh"])
+    entry = {"files": ["k.cu", "h.cuh"], "source_sha": sha, "dram_bytes_per_launch": 1234}
+    (prof / "traffic.json").write_text(json.dumps({"cfg": {"kern": entry}}))
+    assert bench.profiled_traffic("cfg", "kern") == 1234
+    assert bench.profiled_traffic("cfg", "other") is None
+    assert bench.profiled_traffic("nope", "kern") is None
+    (csrc / "h.cuh").write_text("header v2")               # the kernel changed since the capture
+    assert bench.profiled_traffic("cfg", "kern") is None
+    # a file outside the list does not matter
+    (csrc / "h.cuh").write_text("header v1")
+    (csrc / "unrelated.cu").write_text("x")
+    assert bench.profiled_traffic("cfg", "kern") == 1234
+
+
+def test_committed_traffic_entries_are_well_formed():
+    d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for cfg, kernels in d.items():
+        if cfg.startswith("_"):
+            continue
+        for name, e in kernels.items():
+            assert e["dram_bytes_per_launch"] == e["read"] + e["write"], (cfg, name)
+            assert e["files"] and all(os.path.exists(os.path.join(ROOT, "moe_expert_ffn_histogram_gb300",
+                                                                  "csrc", f)) for f in e["files"]), (cfg, name)

@@ -166,7 +166,7 @@ int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, co
     const int cap = rows == 1 ? 1 : group_cap(rows, topk);
     // NVFP4, one token: prefetch the call's whole weight set into L2 when it fits (<= 96 MB,
     // under the 129 MB L2 with room for the rest)
-    if (FMT == 1 && rows == 1 && wd != nullptr && sfd != nullptr) {
+    if (MOE_FP4_L2_PREFETCH && FMT == 1 && rows == 1 && wd != nullptr && sfd != nullptr) {
         const double per_expert = 3.0 * I * (H / 2.0 + H / 16.0);
         if (per_expert * topk <= 96.0 * (1 << 20)) {
             a.l2_prefetch = 1;

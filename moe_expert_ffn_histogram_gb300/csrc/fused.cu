@@ -98,8 +98,8 @@ fused_forward_kernel(const GateUpArgs ga, const DownArgs da, const FusedCtl ctl)
     const int nfb = ga.I / kFeatBlock;
     const int n1 = gl.count * nfb;
     for (int it = blockIdx.x; it < n1; it += gridDim.x) {
-        gate_up_item<FMT, kFusedStagesFp8, kFusedStagesFp4>(ga, gl.g[it / nfb], it % nfb,
-                                                            reinterpret_cast<__half*>(smem_raw), sh);
+        gate_up_item<FMT, kFusedStagesFp8, kFusedStagesFp4, false>(
+            ga, gl.g[it / nfb], it % nfb, reinterpret_cast<__half*>(smem_raw), sh);
         __syncthreads();
     }
 

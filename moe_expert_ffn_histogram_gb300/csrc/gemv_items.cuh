@@ -82,6 +82,7 @@ struct GroupList {
 
 // Small shared scratch of gate_up_item.
 struct GateUpShared {
+    uint4 zeros[2];                        // a zero B fragment pair (single-token NVFP4 path)
     float x_inv[kMaxCols];
     float red[kItemWarps][kMaxCols];
     float a_scale[kMaxCols];
@@ -102,6 +103,44 @@ __device__ __forceinline__ void mma_step_fp8(float (&d)[4], uint32_t qg, uint32_
     mma_f16(d, g_lo, u_lo, g_hi, u_hi, b0, b1);
 }
 
+// One 128-wide super-segment of the single-token NVFP4 gate/up product for lane (g, c) of a warp:
+// the MMA's 8 B columns carry the super-segment's 8 scale groups instead of tokens. In half h
+// lane c's codes belong to group 2c + h; only the lane that holds B column 2c + h at lane c's
+// positions, (g = 2c + h, c), has the token's x there (xh[2h], xh[2h+1]) and every other B value
+// is zero (d[h] collects half h, so the two halves are two independent MMA chains), so D[row][n] is the row's partial dot product over group n, scaled once per
+// (row, group) in fp32 with no per-element multiply. The lane keeps groups 2c and 2c+1 of its
+// gate row and of its up row in accg / accu.
+__device__ __forceinline__ void fp4_token_superseg(const uint4& qg, const uint4& qu, const uint2& fg,
+                                                   const uint2& fu, const uint4 (&xh)[4], int c,
+                                                   int sf_shift, float& accg, float& accu) {
+    const uint32_t wgq[4] = {qg.x, qg.y, qg.z, qg.w};
+    const uint32_t wuq[4] = {qu.x, qu.y, qu.z, qu.w};
+    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // one chain per half
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t ga[8], ua[8];
+        e2m1x8_to_f16x2x4(wgq[2 * h], ga[0], ga[1], ga[2], ga[3]);
+        e2m1x8_to_f16x2x4(wgq[2 * h + 1], ga[4], ga[5], ga[6], ga[7]);
+        e2m1x8_to_f16x2x4(wuq[2 * h], ua[0], ua[1], ua[2], ua[3]);
+        e2m1x8_to_f16x2x4(wuq[2 * h + 1], ua[4], ua[5], ua[6], ua[7]);
+        const uint4 b0 = xh[2 * h], b1 = xh[2 * h + 1];
+        float (&dh)[4] = d[h];                 // half h only feeds the columns 2c' + h
+        mma_f16(dh, ga[0], ua[0], ga[1], ua[1], b0.x, b0.y);
+        mma_f16(dh, ga[2], ua[2], ga[3], ua[3], b0.z, b0.w);
+        mma_f16(dh, ga[4], ua[4], ga[5], ua[5], b1.x, b1.y);
+        mma_f16(dh, ga[6], ua[6], ga[7], ua[7], b1.z, b1.w);
+    }
+    // the scales of groups 2c and 2c+1 of the gate row and of the up row
+    const uint32_t sg = e4m3x2_to_f16x2(((c >> 1) ? fg.y : fg.x) >> sf_shift);
+    const uint32_t su = e4m3x2_to_f16x2(((c >> 1) ? fu.y : fu.x) >> sf_shift);
+    const float2 sgf = __half22float2(*reinterpret_cast<const __half2*>(&sg));
+    const float2 suf = __half22float2(*reinterpret_cast<const __half2*>(&su));
+    accg = fmaf(d[0][0], sgf.x, accg);
+    accg = fmaf(d[1][1], sgf.y, accg);
+    accu = fmaf(d[0][2], suf.x, accu);
+    accu = fmaf(d[1][3], suf.y, accu);
+}
+
 // Dynamic shared memory of the items: x staging [max_cols][H] f16, y rows [P][16] fp32.
 __host__ __device__ inline size_t gate_up_item_smem(int H, int max_cols) {
     return static_cast<size_t>(max_cols) * H * sizeof(__half);
@@ -111,7 +150,9 @@ __host__ __device__ inline size_t down_item_smem(int rows, int topk) {
 }
 
 // ---- gate + up + SwiGLU for (group gv, feature block fb) --------------------------------------
-template <int FMT, int kSF8 = kStagesFp8, int kSF4 = kStagesFp4>
+// kToken1: compile the single-token NVFP4 loop (the stage kernel; the fused batch kernel leaves it
+// out to stay within its register budget and runs one-column groups on the general loop).
+template <int FMT, int kSF8 = kStagesFp8, int kSF4 = kStagesFp4, bool kToken1 = true>
 __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, __half* xs,
                              GateUpShared& sh) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -119,6 +160,9 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
     const int H = a.H, I = a.I;
     const int e = gv.e, ncols = gv.ncols;
     const int topk = a.grp.topk;
+    const int n = fb * kFeatBlock + warp * 8 + g;       // this lane's gate / up row in the block
+
+    if (tid < 2) sh.zeros[tid] = make_uint4(0, 0, 0, 0);   // visible after the staging barriers
 
     // ---- stage the columns' activations as f16 with a per-column power-of-two scale ----
     {
@@ -178,7 +222,6 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
     }
 
     // ---- main loop: 16 MMA rows = 8 gate rows + the same 8 up rows ----
-    const int n = fb * kFeatBlock + warp * 8 + g;
     const bool has_b = g < ncols;
     const __half* xb = xs + static_cast<size_t>(has_b ? g : 0) * H + c * 16;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};   // gate(col 2c), gate(col 2c+1), up(2c), up(2c+1)
@@ -244,6 +287,45 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
         const __half* xb4 = xs + static_cast<size_t>(has_b ? g : 0) * H + c * 32;
         const int nsup = H / 128;
         const int sf_shift = 16 * (c & 1);
+        if (kToken1 && ncols == 1) {
+            // one token: fp4_token_superseg per super-segment, the 4 lanes of a row summed at the end
+            const int act = (g >> 1) == c ? (g & 1) : -1;   // the half whose x this lane carries
+            const __half* xr = xs + c * 32;                   // the token row, lane c's positions
+            // every lane loads its B pair of each half, branch-free: x where it carries that
+            // half, else the zero pair (stride 0)
+            const uint4* xp0 = act == 0 ? reinterpret_cast<const uint4*>(xr) : sh.zeros;
+            const uint4* xp1 = act == 1 ? reinterpret_cast<const uint4*>(xr) + 2 : sh.zeros;
+            const int xst0 = act == 0 ? 16 : 0, xst1 = act == 1 ? 16 : 0;
+            float accg = 0.0f, accu = 0.0f;
+            for (int t0 = 0; t0 < nsup; t0 += kSF4) {
+                uint4 qg[kSF4], qu[kSF4];
+                uint2 fg[kSF4], fu[kSF4];
+#pragma unroll
+                for (int s = 0; s < kSF4; ++s) {
+                    if (t0 + s < nsup) {
+                        qg[s] = ld_stream_v4(pg + (t0 + s) * 64);
+                        qu[s] = ld_stream_v4(pu + (t0 + s) * 64);
+                        fg[s] = ld_stream_v2(fgp + (t0 + s) * 8);
+                        fu[s] = ld_stream_v2(fup + (t0 + s) * 8);
+                    }
+                }
+#pragma unroll
+                for (int s = 0; s < kSF4; ++s) {
+                    const int t = t0 + s;
+                    if (t < nsup) {
+                        const uint4 xh[4] = {xp0[t * xst0], xp0[t * xst0 + 1], xp1[t * xst1],
+                                             xp1[t * xst1 + 1]};
+                        fp4_token_superseg(qg[s], qu[s], fg[s], fu[s], xh, c, sf_shift, accg, accu);
+                    }
+                }
+            }
+            accg += __shfl_xor_sync(0xffffffffu, accg, 1);
+            accg += __shfl_xor_sync(0xffffffffu, accg, 2);
+            accu += __shfl_xor_sync(0xffffffffu, accu, 1);
+            accu += __shfl_xor_sync(0xffffffffu, accu, 2);
+            acc[0] = c == 0 ? accg : 0.0f;                    // column 0 = the token
+            acc[2] = c == 0 ? accu : 0.0f;
+        } else
         for (int t0 = 0; t0 < nsup; t0 += kSF4) {
             uint4 qg[kSF4], qu[kSF4];
             uint2 fg[kSF4], fu[kSF4];

@@ -28,6 +28,11 @@ struct GateUpArgs {
     const uint8_t* pf_sfd; // down scale bytes [E][H][I/16]
 };
 
+// Single-token NVFP4 calls ask L2 for their whole weight set up front (0: they do not).
+#ifndef MOE_FP4_L2_PREFETCH
+#define MOE_FP4_L2_PREFETCH 1
+#endif
+
 // Down projection fused with the slot-order combine (down_combine.cu).
 struct DownArgs {
     int T, H, I, topk, E;

@@ -88,6 +88,13 @@ __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t& r0, uint
         : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(w));
 }
 
+// Two E4M3 bytes (low 16 bits of w: byte 0, byte 1) -> f16x2 {byte 0, byte 1} (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 p, q;\n\tmov.b32 {p, q}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, p;\n\t}" : "=r"(r) : "r"(w));
+    return r;
+}
+
 // One E4M3 scale byte -> {sf, sf} as f16x2.
 __device__ __forceinline__ uint32_t e4m3_splat_f16x2(uint32_t byte) {
     uint32_t r;

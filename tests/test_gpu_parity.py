@@ -71,6 +71,8 @@ SMALL = [
     ("fp8", 3, 640, 256, 12), ("fp8", 5, 256, 128, 20), ("fp8", 8, 384, 256, 24),
     ("fp8", 11, 256, 256, 16), ("fp8", 20, 128, 128, 40),
     ("nvfp4", 1, 256, 128, 16), ("nvfp4", 1, 512, 384, 10), ("nvfp4", 3, 384, 256, 12),
+    # one token: 1, 5 (a batch of 4 and a ragged 1) and 7 (4 + 3) super-segments of 128 along H
+    ("nvfp4", 1, 128, 128, 8), ("nvfp4", 1, 640, 256, 12), ("nvfp4", 1, 896, 128, 9),
     ("nvfp4", 8, 256, 256, 24), ("nvfp4", 13, 256, 128, 16),
 ]
 

@@ -154,9 +154,11 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const fl
     }
     __syncthreads();
     if (threadIdx.x >= 32) return;
-    float picked[kMaxTopk];
+    float picked[kMaxTopk];                          // unrolled to kMaxTopk: stays in registers
     int pid[kMaxTopk];
-    for (int k = 0; k < topk; ++k) {
+#pragma unroll
+    for (int k = 0; k < kMaxTopk; ++k) {
+        if (k >= topk) break;
         float bs = -INFINITY;
         int be = 0x7fffffff;
         for (int e = lane; e < E; e += 32) {
@@ -183,8 +185,12 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const fl
     }
     if (lane == 0) {
         float sum = 0.0f;
-        for (int k = 0; k < topk; ++k) sum += picked[k];
-        for (int k = 0; k < topk; ++k) {
+#pragma unroll
+        for (int k = 0; k < kMaxTopk; ++k)
+            if (k < topk) sum += picked[k];
+#pragma unroll
+        for (int k = 0; k < kMaxTopk; ++k) {
+            if (k >= topk) break;
             const float wv = renorm ? picked[k] / sum : picked[k];
             ids[static_cast<size_t>(t) * topk + k] = pid[k];
             wts[static_cast<size_t>(t) * topk + k] = wv * routed_scale;

@@ -69,3 +69,14 @@ def test_committed_traffic_entries_are_well_formed():
             assert e["dram_bytes_per_launch"] == e["read"] + e["write"], (cfg, name)
             assert e["files"] and all(os.path.exists(os.path.join(ROOT, "moe_expert_ffn_histogram_gb300",
                                                                   "csrc", f)) for f in e["files"]), (cfg, name)
+
+
+def test_cpu_baseline_fills_its_budget():
+    # every seeded route set is run until its share of the budget is used
+    cb = bench.cpu_baseline("tiny_fp8_decode", torch.device("cpu"), budget_s=0.8)
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["cores"] >= 1
+    secs = float(cb["sample"].split(", ")[-1].split()[-2])
+    assert 0.4 <= secs <= 1.6, cb["sample"]
+    toks = int(cb["sample"].split()[0])
+    assert toks >= bench.N_ROUTE_SETS
+    assert abs(cb["value"] - toks / secs) / cb["value"] < 0.1

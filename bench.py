@@ -278,38 +278,95 @@ def hold_stream():
     torch.cuda._sleep(HOLD_CYCLES)
 
 
-def bench_ours(args):
-    from moe_expert_ffn_histogram_gb300 import _build, capi
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    if args.lib:
-        capi._lib = capi.load(args.lib)          # an alternative build of the same library
-    else:
-        _build.build()
-        capi.load()
+# ---- harness statistics ---------------------------------------------------------------------------
 
-    name = args.config
+def nearest_rank(sorted_vals, percentile: int):
+    """The sample at nearest rank ceil(percentile * n / 100) of an ascending list (1 <= percentile
+    <= 100): an observed sample, never an interpolation ("memra-engine 0.108.0
+    src/bin/ep_step_fp8_gate.rs", benchmark harness, `nearest_rank_ns`)."""
+    n = len(sorted_vals)
+    if n == 0 or not 1 <= percentile <= 100:
+        raise ValueError("nearest_rank needs samples and 1 <= percentile <= 100")
+    rank = -(-percentile * n // 100)
+    return sorted_vals[min(max(rank, 1), n) - 1]
+
+
+def step_stats_us(step_ms):
+    """mean, min, p50, p90, p95, p99 and max of the per-step times, in microseconds."""
+    srt = sorted(step_ms)
+    out = {"mean": statistics.mean(srt) * 1e3, "min": srt[0] * 1e3}
+    for q in (50, 90, 95, 99):
+        out[f"p{q}"] = nearest_rank(srt, q) * 1e3
+    out["max"] = srt[-1] * 1e3
+    return {k: round(v, 3) for k, v in out.items()}
+
+
+def output_checksum(values) -> int:
+    """Order- and bit-sensitive 64-bit fold of fp32 values: state = rotl(state, 7) ^ bits(v),
+    starting from 0x9e3779b97f4a7c15 (the gate binary's `output_checksum`, "memra-engine 0.108.0
+    src/bin/ep_step_fp8_gate.rs", benchmark harness). bf16 results are widened to fp32 first.
+    The fold is linear over XOR, so it is evaluated in closed form: v_i enters rotated by
+    7 * (n - 1 - i) and the start value by 7 * n."""
+    a = np.ascontiguousarray(np.asarray(values, dtype=np.float32)).reshape(-1)
+    n = a.size
+    bits = a.view(np.uint32).astype(np.uint64)
+    rot = ((7 * (n - 1 - np.arange(n, dtype=np.int64))) % 64).astype(np.uint64)
+    back = (np.uint64(64) - rot) % np.uint64(64)
+    rotated = (bits << rot) | np.where(rot == 0, np.uint64(0), bits >> back)
+    acc = int(np.bitwise_xor.reduce(rotated)) if n else 0
+    r0 = (7 * n) % 64
+    s0 = 0x9E3779B97F4A7C15
+    s0 = ((s0 << r0) | (s0 >> (64 - r0))) & 0xFFFFFFFFFFFFFFFF if r0 else s0
+    return s0 ^ acc
+
+
+def graded_fraction(alg_bytes, flops, seconds, hbm_gbs, bf16_tflops):
+    """The grouped-GEMM workload's graded fraction: max(bytes / HBM peak, FLOPs / bf16 peak) over
+    the measured time (the roofline of a contraction next to its ridge point)."""
+    floor = max(alg_bytes / (hbm_gbs * 1e9), flops / (bf16_tflops * 1e12))
+    return floor / seconds, floor
+
+
+# ---- our arm ---------------------------------------------------------------------------------------
+
+def prefill_alg_bytes(wl):
+    """Per call of the grouped-GEMM tier: the distinct experts' weights, x and out, the 16-bit
+    activation written and read once per routed pair, ids and weights."""
+    b = alg_bytes(wl)
+    P = wl.T * wl.topk
+    return b["weights"] + 2 * wl.T * wl.H * 2 + 2 * P * wl.I * 2 + P * 8
+
+
+def measure_workload(name, args, dev, bank, world, peak, peak_kind, tpeak, want_router=True):
+    """Times one workload through the C ABI and returns its part of the bench line."""
+    from moe_expert_ffn_histogram_gb300 import capi
     c = inputs.CONFIGS[name]
     E = c["E"] if args.bank_experts is None else args.bank_experts
-    bank = inputs.make_bank(name, dev, experts=None if E == c["E"] else range(E))
     sets = make_route_sets(name, dev, bank, E, args.tokens)
     wl0 = sets[0]
+    T = wl0.T
     fmt_code = capi.FMT_FP8 if c["fmt"] == "fp8" else capi.FMT_NVFP4
-    ws = capi.alloc_workspace(wl0.T, wl0.H, wl0.I, wl0.E, wl0.topk, fmt_code, dev)
-    out = torch.empty(wl0.T, wl0.H, dtype=torch.bfloat16, device=dev)
+    ws = capi.alloc_workspace(T, wl0.H, wl0.I, wl0.E, wl0.topk, fmt_code, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def fwd(wl, o=out):
+    def fwd(wl, o):
         capi.forward(wl.x, wl.ids, wl.wts, wl.bank, wl.limit, out=o, workspace=ws)
 
+    # untimed reference run of every route set (also warm-up): the timed steps must reproduce it
+    refs = []
+    for j in range(N_ROUTE_SETS):
+        flush.zero_()
+        o = torch.empty(T, wl0.H, dtype=torch.bfloat16, device=dev)
+        fwd(sets[j], o)
+        refs.append(o)
+    out = torch.empty(T, wl0.H, dtype=torch.bfloat16, device=dev)
     for i in range(args.warmup):
         flush.zero_()
-        fwd(sets[i % N_ROUTE_SETS])
+        fwd(sets[i % N_ROUTE_SETS], out)
     torch.cuda.synchronize()
+    outs = [torch.empty(T, wl0.H, dtype=torch.bfloat16, device=dev) for _ in range(args.steps)]
 
     # ---- timed region: whole forward per step, device events on the launching stream
     clocks = ClockSampler(dev)
@@ -323,11 +380,18 @@ def bench_ours(args):
         flush.zero_()
         hold_stream()
         ev[i][0].record(stream)
-        fwd(sets[i % N_ROUTE_SETS])
+        fwd(sets[i % N_ROUTE_SETS], outs[i])
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ev]
+    clk = clocks.stop()
+    same = sum(int(torch.equal(outs[i].view(torch.int16), refs[i % N_ROUTE_SETS].view(torch.int16)))
+               for i in range(args.steps))
+    checksum = 0
+    for r in refs:
+        checksum ^= output_checksum(r.float().cpu().numpy())
+    del outs
 
     # ---- the same calls captured once per route set in a CUDA graph and replayed
     graph_ms, graph_err = [], None
@@ -336,7 +400,7 @@ def bench_ours(args):
         for j in range(N_ROUTE_SETS):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                fwd(sets[j])
+                fwd(sets[j], out)
             graphs.append(g)
         torch.cuda.synchronize()
         for i in range(args.warmup + args.steps):
@@ -354,8 +418,7 @@ def bench_ours(args):
         graph_err = f"{type(exc).__name__}: {exc}"[:200]
         torch.cuda.synchronize()
 
-    # ---- the same work as three stage kernels (informational: what fusion saves)
-    T = wl0.T
+    # ---- T <= 8: the same work as three stage kernels (each timed alone)
     stage_ms = {"plan": [], "gate_up": [], "down_combine": []}
     if T <= 8:
         for i in range(args.steps):
@@ -382,20 +445,19 @@ def bench_ours(args):
             for i in range(args.steps):
                 flush.zero_()
                 hold_stream()
-                fwd(sets[i % N_ROUTE_SETS])
+                fwd(sets[i % N_ROUTE_SETS], out)
                 for k, v in capi.stage_times():
                     prefill_stage_ms.setdefault(k, []).append(v)
         finally:
             capi.stage_timing(False)
-    clk = clocks.stop()
 
     # ---- the router in front of the path (informational): a synthetic bf16 router matrix
-    rg = torch.Generator(device=dev)
-    rg.manual_seed(4242)
-    rw = (torch.randn(E, wl0.H, generator=rg, device=dev) * wl0.H ** -0.5).to(torch.bfloat16)
-    rbias = torch.zeros(E, dtype=torch.float32, device=dev)
     router_ms = []
-    if E % 16 == 0 and E <= 1024:
+    if want_router and E % 16 == 0 and E <= 1024:
+        rg = torch.Generator(device=dev)
+        rg.manual_seed(4242)
+        rw = (torch.randn(E, wl0.H, generator=rg, device=dev) * wl0.H ** -0.5).to(torch.bfloat16)
+        rbias = torch.zeros(E, dtype=torch.float32, device=dev)
         rws = torch.empty(int(capi.load().moe_router_workspace_bytes(T, wl0.H, E)), dtype=torch.uint8, device=dev)
         for i in range(args.warmup + args.steps):
             flush.zero_()
@@ -452,48 +514,52 @@ def bench_ours(args):
     e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world, dev)
     e2e_value = sum_over_ranks(float(T * args.steps), world, dev) / e2e_s
 
-    peak, peak_kind = load_peaks()
-    by = [alg_bytes(s) for s in sets]
-    mean_total = statistics.mean(b["total"] for b in by)
+    by = [alg_bytes(s_) for s_ in sets]
+    mean_total = statistics.mean(b_["total"] for b_ in by)
     ms = statistics.mean(step_ms)
     call_gbs = mean_total / (ms * 1e-3) / 1e9
-    # T = 1: two kernels (gate_up, then down_combine as a programmatic dependent launch);
-    # 2 <= T <= 8: one fused cooperative kernel after a 4-byte memset of its barrier word, so the
-    # dominant kernel is the whole step; T > 8: the prefill tier (tensor-bound GEMMs).
-    if T == 1 and stage_ms["gate_up"]:
+    if T == 1:
         # dominant kernel: gate_up_kernel (two thirds of the bytes), timed by its own CUDA events
         # in the stage loop above (launched alone, so without the PDL overlap of the step)
         gu_ms = statistics.mean(stage_ms["gate_up"])
-        gu_bytes = statistics.mean(b["gate_up"] for b in by)
+        dn_ms = statistics.mean(stage_ms["down_combine"])
+        gu_bytes = statistics.mean(b_["gate_up"] for b_ in by)
+        dn_bytes = statistics.mean(b_["down"] for b_ in by)
         ach = gu_bytes / (gu_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "gate_up_kernel", "achieved": round(ach, 1), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "traffic": profiled_traffic(name, "gate_up"), "alg_bytes_per_launch": int(gu_bytes),
                 "avg_launch_us": round(gu_ms * 1e3, 2),
+                "down": {"kernel": "down_combine_kernel", "alg_bytes_per_launch": int(dn_bytes),
+                         "avg_launch_us": round(dn_ms * 1e3, 2),
+                         "achieved": round(dn_bytes / (dn_ms * 1e-3) / 1e9, 1),
+                         "frac": round(dn_bytes / (dn_ms * 1e-3) / 1e9 / peak, 4)},
                 "step": {"kernels": "gate_up_kernel + down_combine_kernel (PDL)",
                          "alg_bytes": int(mean_total), "achieved": round(call_gbs, 1),
                          "frac": round(call_gbs / peak, 4)},
                 "note": "CUDA events on the launching stream"}
+        launches_per_step = 2
     elif T <= 8:
-        kname, note = "fused_forward_kernel", "step = barrier memset + the fused kernel"
         ach = mean_total / (ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": kname, "achieved": round(ach, 1), "peak": peak,
+        roof = {"bound": "hbm", "kernel": "fused_forward_kernel", "achieved": round(ach, 1), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "traffic": profiled_traffic(name, "fused"), "alg_bytes_per_launch": int(mean_total),
-                "avg_launch_us": round(ms * 1e3, 2), "note": note + " (CUDA events)"}
-    if T <= 8:
-        launches_per_step = 2 if T == 1 else 1
+                "avg_launch_us": round(ms * 1e3, 2),
+                "note": "step = barrier memset + the fused kernel (CUDA events); bytes over the "
+                        "realised union of each route set"}
+        launches_per_step = 1
     else:
         # dominant kernel: the gate/up grouped GEMM (two thirds of the flops), timed by the
         # library's stage events; every (token, slot) pair is one GEMM row
         P = T * 8
-        gu_flops = 2.0 * 2 * P * c["H"] * c["I"]
-        dn_flops = 2.0 * P * c["H"] * c["I"]
-        tpeak = load_tensor_peak()
+        gu_flops = 2.0 * 2 * P * wl0.H * wl0.I
+        dn_flops = 2.0 * P * wl0.H * wl0.I
         gu_ms = statistics.mean(prefill_stage_ms["gate_up_gemm"])
         dn_ms = statistics.mean(prefill_stage_ms["down_gemm"])
         ach = gu_flops / (gu_ms * 1e-3) / 1e12
         step_tf = (gu_flops + dn_flops) / (ms * 1e-3) / 1e12
+        pb = statistics.mean(prefill_alg_bytes(s_) for s_ in sets)
+        graded, floor_s = graded_fraction(pb, gu_flops + dn_flops, ms * 1e-3, peak, tpeak)
         roof = {"bound": "tensor", "kernel": "prefill_tw_gemm_kernel (gate/up)",
                 "achieved": round(ach, 1), "peak": tpeak, "peak_kind": "measured bf16 dense burst",
                 "unit": "TFLOP/s", "frac": round(ach / tpeak, 4),
@@ -505,10 +571,13 @@ def bench_ours(args):
                          "frac": round(dn_flops / (dn_ms * 1e-3) / 1e12 / tpeak, 4),
                          "traffic": profiled_traffic(name, "down_gemm")},
                 "step": {"alg_flops": gu_flops + dn_flops, "achieved": round(step_tf, 1),
-                         "frac": round(step_tf / tpeak, 4), "hbm_bytes": int(mean_total),
-                         "hbm_frac": round(mean_total / (ms * 1e-3) / 1e9 / peak, 4),
+                         "frac": round(step_tf / tpeak, 4), "hbm_bytes": int(pb),
+                         "hbm_frac": round(pb / (ms * 1e-3) / 1e9 / peak, 4),
                          "stages_us": {k: round(statistics.mean(v) * 1e3, 1)
                                        for k, v in prefill_stage_ms.items()}},
+                "graded": {"frac": round(graded, 4), "floor_us": round(floor_s * 1e6, 1),
+                           "rule": "max(alg bytes / HBM peak, FLOPs / bf16 peak) / step time",
+                           "target_frac": 0.5},
                 "note": "f16 x f16 -> f32 MMA (same nominal rate as bf16); kernel times from the "
                         "library's stage events on the launching stream"}
         # route plan (three launches from 4096 pairs on), tile list, x prep, gate/up GEMM,
@@ -516,21 +585,21 @@ def bench_ours(args):
         launches_per_step = ((3 if P >= 4096 else 1) + 5
                              + (0 if math.isfinite(inputs.LIMIT) and inputs.LIMIT <= 255 else 1))
 
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+    return {
+        "workload": name, "value": round(value, 2), "unit": UNIT, "ms_per_step": round(ms, 5),
         "dtype": "e4m3/bf16->f32" if c["fmt"] == "fp8" else "e2m1/bf16->f32",
-        "data": "synthetic (seeded N(0,0.02) weights quantised, N(0,1) bf16 activations)",
-        "config": {"workload": name, "T": T, "H": c["H"], "I": c["I"], "E": E, "topk": 8,
+        "config": {"workload": name, "T": T, "H": wl0.H, "I": wl0.I, "E": E, "topk": 8,
                    "format": "fp8_e4m3_block128" if c["fmt"] == "fp8" else "nvfp4",
                    "routes": c["routes"], "route_sets": N_ROUTE_SETS,
                    "l2": "flushed between steps (write of 2x L2 outside the timed events)",
                    "parallelism": f"replicas x{world}"},
         "effective_weight_gbs": round(call_gbs, 1),
         "hbm_frac_of_peak": round(call_gbs / peak, 4),
-        "p50_ms": round(float(np.percentile(step_ms, 50)), 5),
-        "p99_ms": round(float(np.percentile(step_ms, 99)), 5),
+        "step_us": step_stats_us(step_ms),
+        "output_check": {"bit_identical_steps": same, "steps": args.steps,
+                         "against": "an untimed run of the same route set before the timed region",
+                         "checksum": f"{checksum:016x}",
+                         "checksum_of": "XOR over the 8 route sets of the gate binary's output fold"},
         "stage_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in stage_ms.items() if v},
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,
@@ -545,6 +614,71 @@ def bench_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 5)},
         "clocks": clk,
+    }
+
+
+SIDE_WORKLOADS = ("fp8_batchm", "nvfp4_decode", "fp8_prefill", "nvfp4_prefill")
+
+
+def bench_ours(args):
+    from moe_expert_ffn_histogram_gb300 import _build, capi
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if args.lib:
+        capi._lib = capi.load(args.lib)          # an alternative build of the same library
+    else:
+        _build.build()
+        capi.load()
+    peak, peak_kind = load_peaks()
+    tpeak = load_tensor_peak()
+    banks = {}
+
+    def bank_for(name):
+        c = inputs.CONFIGS[name]
+        key = (c["fmt"], c["bank_seed"], args.bank_experts)
+        if key not in banks:
+            banks.clear()                          # one resident bank at a time
+            torch.cuda.empty_cache()
+            E = c["E"] if args.bank_experts is None else args.bank_experts
+            banks[key] = inputs.make_bank(name, dev, experts=None if E == c["E"] else range(E))
+        return banks[key]
+
+    name = args.config
+    head = measure_workload(name, args, dev, bank_for(name), world, peak, peak_kind, tpeak)
+    side = {}
+    todo = [w for w in (args.workloads.split(",") if args.workloads else []) if w and w != name]
+    # group by bank so that each bank is generated once
+    todo.sort(key=lambda w: (inputs.CONFIGS[w]["fmt"] != inputs.CONFIGS[name]["fmt"], w))
+    for w in todo:
+        r = measure_workload(w, args, dev, bank_for(w), world, peak, peak_kind, tpeak)
+        side[w] = {k: r[k] for k in ("value", "unit", "ms_per_step", "dtype", "config", "step_us",
+                                     "effective_weight_gbs", "hbm_frac_of_peak", "roofline", "e2e",
+                                     "output_check", "stage_us", "gpu_launches", "graph", "router",
+                                     "clocks")}
+
+    result = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": head["dtype"],
+        "data": "synthetic (seeded N(0,0.02) weights quantised, N(0,1) bf16 activations)",
+        "config": head["config"],
+        "effective_weight_gbs": head["effective_weight_gbs"],
+        "hbm_frac_of_peak": head["hbm_frac_of_peak"],
+        "p50_ms": round(head["step_us"]["p50"] / 1e3, 5),
+        "p99_ms": round(head["step_us"]["p99"] / 1e3, 5),
+        "step_us": head["step_us"],
+        "output_check": head["output_check"],
+        "stage_us": head["stage_us"],
+        "roofline": head["roofline"],
+        "gpu_launches": head["gpu_launches"],
+        "graph": head["graph"],
+        "router": head["router"],
+        "e2e": head["e2e"],
+        "clocks": head["clocks"],
+        "workloads": side,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(name, dev, budget_s=args.cpu_budget)
@@ -603,6 +737,9 @@ def main(argv=None):
                     help="use only the first N experts of the bank (small profiling captures)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count T (small profiling captures)")
+    ap.add_argument("--workloads", default=",".join(SIDE_WORKLOADS),
+                    help="comma-separated further workloads measured in the same run and reported "
+                         "under 'workloads' ('' for none)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps, always
     if args.impl == "reference":

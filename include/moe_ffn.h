@@ -16,8 +16,10 @@
  *
  * Conventions shared by every entry point:
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except where a comment
- *     says otherwise. The library allocates nothing, owns nothing, and keeps no state between
- *     calls. Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     says otherwise. No call allocates memory. The only state the library keeps between calls
+ *     is the scratch array of moe_fp8_forward_noalloc (and its cached device address), a few
+ *     per-device launch parameters it caches, and the switches of moe_stage_timing and
+ *     moe_test_barrier_timeout. Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
  *     stream) and the function returns after enqueueing; nothing is synchronised.
  *   - Argument checks are synchronous: on any MOE_ERR_* return nothing has been enqueued, except
  *     MOE_ERR_CUDA, which reports a launch failure (work before the failing launch may be queued).
@@ -64,9 +66,16 @@ typedef enum {
 } moe_format;
 
 #define MOE_ERRBIT_BAD_ID 1
-/* A grid-wide barrier of the fused forward gave up after ~2 s (possible only if the GPU could not
- * keep all CTAs of the cooperative launch resident); the output of that call is incomplete. */
+/* A bounded wait gave up (about 1-2 s of SM clock): the grid-wide barrier of the cooperative
+ * forward (possible only if the GPU could not keep all of its CTAs resident) or a pipeline wait of
+ * the grouped-GEMM tier. The output of that call is invalid. The cooperative forward writes NaN to
+ * the output rows of every CTA that gave up, so the failure shows in `out` even when err is NULL;
+ * the grouped-GEMM tier leaves the rows of the tiles it abandoned unwritten and reports the
+ * failure only through *err. */
 #define MOE_ERRBIT_BARRIER 2
+/* After such an abort, a grouped-GEMM CTA's wait for its own TMA loads and MMAs in flight also
+ * timed out before it released its shared and tensor memory. */
+#define MOE_ERRBIT_DRAIN 4
 
 /*
  * moe_workspace_bytes - device scratch needed by moe_fp8_forward / moe_nvfp4_forward for a call
@@ -243,7 +252,9 @@ MOE_API int moe_nvfp4_down_combine(int T, int H, int I, int E, int topk, const i
  * needs to start at zero. Calls that overlap on the GPU race on it: serialise them.
  * The first call on each device (with that device current) looks up the array's device address
  * with cudaGetSymbolAddress, which may load the library's kernels; make it before any stream
- * capture. No cudaMalloc, cudaFree or allocating library routine is ever called.
+ * capture. The address is kept per device and per CUDA context: after cudaDeviceReset() the next
+ * call on that device looks it up again (make that call outside a capture too). No cudaMalloc,
+ * cudaFree or allocating library routine is ever called.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
 MOE_API int moe_fp8_forward_noalloc(const uint16_t* x, int T, int H, int I, int E, int topk,
@@ -265,7 +276,9 @@ MOE_API int moe_fp8_forward_noalloc(const uint16_t* x, int T, int H, int I, int 
  *   logits       [T][E] fp32 out (device) or NULL: l = sum_h x[t][h] * router_w[e][h], fp32 MMA
  *                accumulation.
  *   topk_ids     [T][topk] int32 out: experts by descending sigmoid(l) + bias; equal scores go to
- *                the lower expert index (the pages print no tie rule; this is the stable one).
+ *                the lower expert index (the pages print no tie rule; this is the stable one). The
+ *                ids of a token are always distinct and in [0, E): a -inf score is picked only
+ *                after every finite one, a NaN score (NaN logit or bias) only after every number.
  *   topk_weights [T][topk] fp32 out: sigmoid(l) of each pick (the bias only selects), divided by
  *                the sum over the picks if renormalize != 0, times routed_scale.
  *   workspace    >= moe_router_workspace_bytes(T, H, E) bytes (device, 256-byte aligned): partial
@@ -310,6 +323,15 @@ MOE_API int moe_shared_expert_bf16(const uint16_t* x, int T, int H, int S, const
  */
 MOE_API int moe_stage_timing(int enable);
 MOE_API int moe_stage_times(float* ms, const char** names, int max_stages);
+
+/*
+ * moe_test_barrier_timeout - test hook, off by default. While enabled (enable != 0), every
+ * cooperative forward (2 <= T <= 8 rows per sweep) makes its grid-wide barrier wait for one CTA
+ * more than the grid holds and gives up after about 10 ms instead of about 2 s, so that a test can
+ * check the timeout path without a GPU fault: MOE_ERRBIT_BARRIER is set in *err, `out` holds NaN,
+ * and the CUDA context stays usable. Returns MOE_OK. Process-wide; not for production calls.
+ */
+MOE_API int moe_test_barrier_timeout(int enable);
 
 /* Library build identification: the compiled CUDA architecture string (e.g. "sm_103a"). */
 MOE_API const char* moe_build_arch(void);

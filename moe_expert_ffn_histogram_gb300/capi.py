@@ -21,13 +21,15 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_WOR
 FMT_FP8 = 1
 FMT_NVFP4 = 2
 ERRBIT_BAD_ID = 1
+ERRBIT_BARRIER = 2
+ERRBIT_DRAIN = 4
 
 EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_nvfp4_forward",
             "moe_plan", "moe_fp8_gate_up", "moe_fp8_down_combine", "moe_nvfp4_gate_up",
             "moe_nvfp4_down_combine", "moe_build_arch", "moe_fp8_forward_noalloc",
             "moe_router_workspace_bytes", "moe_router", "moe_fp8_forward_layer",
             "moe_nvfp4_forward_layer", "moe_shared_expert_workspace_bytes", "moe_shared_expert_bf16",
-            "moe_stage_timing", "moe_stage_times")
+            "moe_stage_timing", "moe_stage_times", "moe_test_barrier_timeout")
 
 _lib = None
 
@@ -94,6 +96,8 @@ def load(path: Optional[str] = None):
     lib.moe_shared_expert_bf16.argtypes = [vp, i32, i32, i32, vp, vp, vp, f32, vp, vp, sz, vp]
     lib.moe_stage_timing.restype = i32
     lib.moe_stage_timing.argtypes = [i32]
+    lib.moe_test_barrier_timeout.restype = i32
+    lib.moe_test_barrier_timeout.argtypes = [i32]
     lib.moe_stage_times.restype = i32
     lib.moe_stage_times.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), i32]
     if path is None:
@@ -318,6 +322,11 @@ def down_combine(ids, wts, bank, out, workspace, stream=None):
                                         _ptr(workspace), workspace.numel(),
                                         _stream(out.device, stream))
     _check("moe_*_down_combine", rc)
+
+
+def test_barrier_timeout(enable: bool) -> None:
+    """moe_test_barrier_timeout: make the cooperative forward's grid barrier time out (test hook)."""
+    _check("moe_test_barrier_timeout", load().moe_test_barrier_timeout(1 if enable else 0))
 
 
 def build_arch() -> str:

@@ -8,8 +8,10 @@
 //                 programmatic dependent that starts its weight stream while gate_up drains.
 //   2 <= T <= 8 : one fused cooperative launch (fused.cu): in-kernel expert grouping, gate/up +
 //                 SwiGLU, grid barrier, down + slot-order combine (after a 4-byte barrier memset).
-//   T > 8, FP8  : grouped GEMMs over expert-sorted rows (prefill.cu).
-//   T > 8, NVFP4: even row groups of <= 8 tokens ("forward.rs", `moe_row_groups`), each as above.
+//   8 < T < the measured crossover (28 FP8, 18 NVFP4): even row groups of <= 8 tokens
+//                 ("forward.rs", `moe_row_groups`), each through the cooperative kernel.
+//   from the crossover on: grouped GEMMs over expert-sorted rows on the tcgen05 tensor cores
+//                 (prefill.cu; NVFP4 needs H and I multiples of 256, else it keeps the sweeps).
 // The stage entry points (moe_plan, moe_*_gate_up, moe_*_down_combine) run the same work items
 // as separate kernels and give the same bits.
 #include <cmath>
@@ -41,10 +43,9 @@ bool shape_ok(int T, int H, int I, int E, int topk) {
 
 int rows_per_sweep(int T) { return T < kMaxRowsPerSweep ? T : kMaxRowsPerSweep; }
 
-// The grouped-GEMM (prefill) tier: FP8 weights, more than one 8-token sweep, and shapes its
-// tiles cover (per-K-block scale tables of <= 64 entries).
-// Smallest T the grouped-GEMM tier takes; below it, sweeps of <= 8 tokens through the cooperative
-// kernel. Measured on GB300 with the decode banks (uniform routes over 256 / 160 experts, L2
+// The grouped-GEMM (prefill) tier: more than one 8-token sweep, and shapes its tiles cover
+// (per-K-block scale tables of <= 64 entries). Smallest T the grouped-GEMM tier takes; below it,
+// sweeps of <= 8 tokens through the cooperative kernel. Measured on GB300 with the decode banks (uniform routes over 256 / 160 experts, L2
 // flushed): FP8 sweeps win up to T = 24 (1.57 vs 1.69 ms) and lose from T = 32 (2.11 vs
 // 2.02 ms); NVFP4 sweeps win at T = 16 (0.57 vs 0.60 ms) and lose from T = 24 (0.86 vs 0.76 ms).
 #ifndef MOE_PREFILL_MIN_T
@@ -580,6 +581,11 @@ int moe_shared_expert_bf16(const uint16_t* x, int T, int H, int S, const uint16_
         reinterpret_cast<const __nv_bfloat16*>(w_up), reinterpret_cast<const __nv_bfloat16*>(w_down), limit,
         reinterpret_cast<__nv_bfloat16*>(out), static_cast<uint8_t*>(workspace), sms,
         static_cast<cudaStream_t>(stream)));
+}
+
+int moe_test_barrier_timeout(int enable) {
+    set_test_barrier_timeout(enable != 0);
+    return MOE_OK;
 }
 
 const char* moe_build_arch(void) { return "sm_103a"; }

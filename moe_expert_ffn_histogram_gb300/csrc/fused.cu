@@ -8,8 +8,14 @@
 // The barrier counter lives in the workspace and is zeroed by a memset on the same stream right
 // before the launch. The wait is bounded: if it ever exceeds ~2 s of SM clock (possible only if the
 // GPU could not keep every CTA resident, which the cooperative launch rules out), the CTA sets
-// MOE_ERRBIT_BARRIER in the error word and returns instead of hanging.
+// MOE_ERRBIT_BARRIER in the error word, writes NaN to the output rows it owns (so an incomplete
+// result is visible even to a caller that passed no error word) and returns instead of hanging.
+// moe_test_barrier_timeout() makes the barrier wait for one CTA more than the grid holds, with a
+// ~10 ms bound, so that a test can drive that path.
+#include <atomic>
 #include <mutex>
+
+#include "../../include/moe_ffn.h"
 
 #include "gemv_items.cuh"
 
@@ -22,7 +28,8 @@ namespace moe {
 namespace {
 
 constexpr long long kBarrierTimeoutCycles = 1ll << 32;
-constexpr int kErrBitBarrier = 2;
+constexpr long long kTestBarrierTimeoutCycles = 1ll << 24;   // ~10 ms: the test hook's bound
+constexpr int kErrBitBarrier = MOE_ERRBIT_BARRIER;
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
@@ -30,8 +37,9 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
-// Grid-wide barrier over gridDim.x CTAs on a zeroed counter; false on timeout.
-__device__ bool grid_barrier(unsigned* counter, int32_t* err) {
+// Grid-wide barrier over gridDim.x CTAs (plus `extra`, which only the test hook sets) on a zeroed
+// counter; false after `limit` cycles of SM clock.
+__device__ bool grid_barrier(unsigned* counter, int32_t* err, unsigned extra, long long limit) {
     __shared__ int ok;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -39,8 +47,8 @@ __device__ bool grid_barrier(unsigned* counter, int32_t* err) {
         atomicAdd(counter, 1u);
         const long long t0 = clock64();
         int good = 1;
-        while (ld_acquire_gpu(counter) < gridDim.x) {
-            if (clock64() - t0 > kBarrierTimeoutCycles) {
+        while (ld_acquire_gpu(counter) < gridDim.x + extra) {
+            if (clock64() - t0 > limit) {
                 good = 0;
                 break;
             }
@@ -60,6 +68,8 @@ struct FusedCtl {
     unsigned* barrier;   // zeroed before the launch
     int rows;            // tokens of this sub-batch (1..8)
     int cap;             // columns per group
+    unsigned barrier_extra;        // 0; 1 under the test hook (the barrier can never complete)
+    long long barrier_limit;       // wait bound in SM clock cycles
 };
 
 template <int FMT>
@@ -114,7 +124,15 @@ fused_forward_kernel(const GateUpArgs ga, const DownArgs da, const FusedCtl ctl)
             prefetch_l2(da.sfd + r0 * (da.I / 16), static_cast<uint32_t>(kDownRows * (da.I / 16)));
     }
 
-    if (!grid_barrier(ctl.barrier, ga.err)) return;
+    if (!grid_barrier(ctl.barrier, ga.err, ctl.barrier_extra, ctl.barrier_limit)) {
+        // the rows this CTA would have written (down items jt = blockIdx.x + i * gridDim.x, no
+        // other CTA writes them) become NaN: the call's output is invalid, and visibly so
+        const __nv_bfloat16 qnan = __ushort_as_bfloat16(0x7FC0);
+        for (int jt = blockIdx.x; jt < n2; jt += gridDim.x)
+            for (int i = threadIdx.x; i < da.T * kDownRows; i += blockDim.x)
+                da.out[static_cast<size_t>(i / kDownRows) * da.H + jt * kDownRows + i % kDownRows] = qnan;
+        return;
+    }
 
     // ---- phase 2: down + slot-order combine items (16 output rows each) ----
     for (int jt = blockIdx.x; jt < n2; jt += gridDim.x) {
@@ -124,6 +142,8 @@ fused_forward_kernel(const GateUpArgs ga, const DownArgs da, const FusedCtl ctl)
 }
 
 namespace {
+
+std::atomic<int> g_test_barrier_timeout{0};
 
 // Co-resident CTAs per SM for a (kernel, dynamic smem) pair, times the SM count; cached per
 // device because the occupancy query costs host time on every call.
@@ -176,7 +196,9 @@ cudaError_t launch_fused_forward(const GateUpArgs& ga, const DownArgs& da, unsig
     int grid = 0;
     if ((st = fused_grid<FMT>(smem, &grid)) != cudaSuccess) return st;
     if ((st = cudaMemsetAsync(barrier, 0, sizeof(unsigned), stream)) != cudaSuccess) return st;
-    FusedCtl ctl{barrier, rows, cap};
+    const bool test_timeout = g_test_barrier_timeout.load(std::memory_order_relaxed) != 0;
+    FusedCtl ctl{barrier, rows, cap, test_timeout ? 1u : 0u,
+                 test_timeout ? kTestBarrierTimeoutCycles : kBarrierTimeoutCycles};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kItemThreads);
@@ -190,6 +212,8 @@ cudaError_t launch_fused_forward(const GateUpArgs& ga, const DownArgs& da, unsig
     if ((st = cudaLaunchKernelEx(&cfg, fused_forward_kernel<FMT>, ga, da, ctl)) != cudaSuccess) return st;
     return cudaGetLastError();
 }
+
+void set_test_barrier_timeout(bool on) { g_test_barrier_timeout.store(on ? 1 : 0); }
 
 template cudaError_t launch_fused_forward<0>(const GateUpArgs&, const DownArgs&, unsigned*, int, int,
                                              cudaStream_t);

@@ -64,6 +64,8 @@ template <int FMT> cudaError_t launch_fused_forward(const GateUpArgs& ga, const 
                                                     unsigned* barrier, int rows, int cap,
                                                     cudaStream_t stream);
 size_t fused_smem_bytes(int H, int rows, int topk, int cap);
+// Test hook of the fused kernel's grid barrier (moe_test_barrier_timeout).
+void set_test_barrier_timeout(bool on);
 
 // Wide tier (prefill.cu): workspace layout and the launch sequence of the grouped-GEMM path.
 struct PrefillLayout {

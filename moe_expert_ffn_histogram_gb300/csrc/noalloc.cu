@@ -18,9 +18,13 @@
 //     stream, or events).
 //   * The first call on each device, with that device current, looks up the array's device
 //     address with cudaGetSymbolAddress (which may load the library's kernels on that device).
-//     Make that first call before any stream capture.
+//     Make that first call before any stream capture. The address is cached per device and per
+//     CUDA context: after cudaDeviceReset() the device gets a new context, the next call looks the
+//     address up again (so, again, make it outside a capture).
 //   * No cudaMalloc, cudaFree or allocating library routine is called.
 // The pages have no counterpart to this entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -36,6 +40,32 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 std::mutex g_setup_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // id of the context the address belongs to
+
+// Unique id of the calling thread's current CUDA context (0 if the driver cannot tell): a reset
+// device gets a new context and so a new id.
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Device address of the scratch array on the current device (host code must not use the
 // array's name as a pointer: on the host it is only a stand-in for the symbol).
@@ -43,12 +73,17 @@ int scratch_on_current_device(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    // a thread that has not used the runtime yet has no current context (id 0): the lookup then
+    // runs once more, which makes the device's primary context current, and the id read after it
+    // is the one kept
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (g_scratch_ptr[dev] == nullptr || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         const cudaError_t st = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (st != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = current_context_id();
     }
     *out = g_scratch_ptr[dev];
     return MOE_OK;

@@ -32,8 +32,11 @@
 // The slice is 128 wide because every slice costs the converters, the watcher and the MMA warp
 // a fixed round of barrier traffic (~500 cycles measured for an empty pipeline of this shape);
 // 128-wide slices double the MMA work that pays for it.
-// Every wait is bounded (~1 s of SM clock); on a timeout the CTA sets bit 1 of the error word,
-// every role leaves its loop, and the CTA frees its TMEM and exits.
+// Every wait is bounded (~1 s of SM clock); on a timeout the CTA sets bit 1 of the error word and
+// every role leaves its loop; the producers issue no further box once any role has given up. The
+// CTA then waits (bounded again) until every TMA box it issued has landed and every MMA it queued
+// has completed, and only then frees its TMEM and exits, so that no asynchronous write reaches
+// its shared memory or TMEM after it has gone (if that drain also times out: bit 2 as well).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -114,7 +117,10 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     // boxes when those are not on their own - may be refilled); acc_full/acc_empty[b]:
     // accumulator b complete / drained.
     __shared__ __align__(8) uint64_t tfull[NT], tempty[NT], afull[NS], sempty[NS], rfull[NR], rempty[NR], acc_full[2],
-        acc_empty[2];
+        acc_empty[2], mma_done;
+    // boxes issued into each token slot / raw stage so far: the phase of the last one is what
+    // the teardown waits for after an abort
+    __shared__ volatile uint32_t tok_issued[NT], raw_issued[NR];
     __shared__ uint32_t w_scale[kTwConvWarps][64];       // per converter warp: its rows' scale table
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
@@ -142,6 +148,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], kTwEpiWarps);
         }
+        mbar_init(&mma_done, 1);
+        for (int t = 0; t < NT; ++t) tok_issued[t] = 0;
+        for (int r = 0; r < NR; ++r) raw_issued[r] = 0;
         abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;");
     }
@@ -171,6 +180,10 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt, ++sc) {
                     if (static_cast<int>(sc % 2) != pw) continue;
+                    if (abort_s) {                             // another role gave up: issue no more
+                        ok = false;
+                        break;
+                    }
                     if (tok) {
                         const uint32_t s = sc % NT, u = sc / NT;
                         if (u > 0 && !tw_wait(Cfg::kTokOwn ? &tempty[s] : &sempty[s], (u - 1) & 1u)) {
@@ -181,6 +194,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                         mbar_arrive_expect_tx(&tfull[s], kTwTok);
                         tma_load_2d(smem_u32(stTok(s)), &tmTok, kt * kTwSliceK, r0, &tfull[s]);
                         tma_load_2d(smem_u32(stTok(s)) + kTwBox, &tmTok, kt * kTwSliceK + 64, r0, &tfull[s]);
+                        tok_issued[s] = u + 1;
                     } else {
                         const uint32_t r = sc % NR, u = sc / NR;
                         if (u > 0 && !tw_wait(&rempty[r], (u - 1) & 1u)) {
@@ -192,6 +206,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                         if (NM == 2)
                             tma_load_2d(smem_u32(stRaw(r)) + 128 * Cfg::kRowBytes, &tmW1, kt * Cfg::kRowBytes, wy,
                                         &rfull[r]);
+                        raw_issued[r] = u + 1;
                     }
                 }
                 if (!ok) {
@@ -395,6 +410,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
             }
             ++tcount;
         }
+        // one more commit: it arrives once every MMA this thread queued has completed (the
+        // teardown waits for it before TMEM and shared memory are released)
+        if (lane == 0) mma_commit(&mma_done);
     } else if (warp == kTwWatchWarp) {
         // ---------------- watcher ----------------
         // Per slice: the accumulator drained (first slice of a tile), the token boxes landed and
@@ -419,6 +437,10 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                     ok = !abort_s;
                     if (ok && kt == 0 && v > 0) ok = tw_wait(&acc_empty[b], (v - 1) & 1u);
                     if (ok) ok = tw_wait(&tfull[t], ut & 1u) && tw_wait(&afull[s], us & 1u);
+                    if (!ok) {                                 // stop the producers before the MMA
+                        abort_s = 1;                           // warp is released without operands
+                        __threadfence_block();
+                    }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (kt == 0) {
@@ -521,12 +543,24 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     }
 
     // ---------------- teardown ----------------
+    // Every role has left its loop. Without an abort every box issued was waited for by its
+    // consumer and every MMA by the epilogue; after one, boxes may still be landing and MMAs still
+    // running, so the CTA waits for the last phase of each token slot and raw stage that received
+    // a box, and for the MMA warp's final commit, before TMEM and shared memory are released.
     __syncthreads();
-    if (abort_s) {                                        // let any MMA still in flight finish
-        if (tid == 0 && p.err != nullptr) atomicOr(p.err, 2);
-        const long long t0 = clock64();
-        while (clock64() - t0 < (1ll << 22)) {
+    {
+        bool drained = true;
+        if (tid == 0) {
+            drained = tw_wait(&mma_done, 0);
+        } else if (abort_s && tid <= NT) {
+            const uint32_t n = tok_issued[tid - 1];
+            if (n > 0) drained = tw_wait(&tfull[tid - 1], (n - 1) & 1u);
+        } else if (abort_s && tid <= NT + NR) {
+            const uint32_t n = raw_issued[tid - 1 - NT];
+            if (n > 0) drained = tw_wait(&rfull[tid - 1 - NT], (n - 1) & 1u);
         }
+        if (abort_s && tid == 0 && p.err != nullptr) atomicOr(p.err, 2);
+        if (!drained && p.err != nullptr) atomicOr(p.err, 4);
     }
     tc_fence_before();
     __syncthreads();

@@ -15,8 +15,9 @@
 //     tokens per CTA so that the matrix is re-read from L2 once per 32 tokens.
 //   router_topk_kernel: one CTA per token sums the K parts in order and computes sigmoid and score
 //     for every expert; its first warp selects top-k by repeated warp arg-max (score descending,
-//     ties to the lower expert index); weights are the picks' sigmoids (renormalised in pick
-//     order, times routed_scale).
+//     ties to the lower expert index, NaN scores after every number) over the experts not yet
+//     taken (a flag per expert, so a -inf or NaN score never makes an index invalid); weights are
+//     the picks' sigmoids (renormalised in pick order, times routed_scale).
 #include "kernels.cuh"
 
 namespace moe {
@@ -132,6 +133,17 @@ __global__ void __launch_bounds__(kRtSmallWarps * 32) dense_small_kernel(const _
     }
 }
 
+// Selection order of the top-k scan: a higher score first, equal scores to the lower expert index,
+// and a NaN score after every number (a NaN logit or bias cannot pick an expert ahead of a finite
+// or infinite score; NaN scores among themselves go by index). `be` < 0 means no candidate yet.
+__device__ __forceinline__ bool topk_better(float v, int e, float bs, int be) {
+    if (be < 0) return true;
+    const bool vn = isnan(v), bn = isnan(bs);
+    if (vn != bn) return bn;
+    if (vn) return e < be;
+    return v > bs || (v == bs && e < be);
+}
+
 __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const float* __restrict__ part, int KS,
                                                                         int T, int E, const float* __restrict__ bias,
                                                                         int topk, float routed_scale, int renorm,
@@ -139,10 +151,11 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const fl
                                                                         int32_t* __restrict__ ids,
                                                                         float* __restrict__ wts) {
     // one CTA per token: all its threads sum the K parts and score the experts, warp 0 selects
-    extern __shared__ float rt_smem[];                // [2][E]: sigmoid, score
+    extern __shared__ float rt_smem[];                // [2][E] fp32: sigmoid, score; then [E] taken flags
     const int lane = threadIdx.x & 31, t = blockIdx.x;
     float* sig = rt_smem;
     float* score = sig + E;
+    unsigned char* taken = reinterpret_cast<unsigned char*>(score + E);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float l = 0.0f;
 #pragma unroll 8
@@ -151,6 +164,7 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const fl
         const float s = 1.0f / (1.0f + expf(-l));
         sig[e] = s;
         score[e] = s + (bias != nullptr ? bias[e] : 0.0f);
+        taken[e] = 0;
     }
     __syncthreads();
     if (threadIdx.x >= 32) return;
@@ -159,11 +173,14 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const fl
 #pragma unroll
     for (int k = 0; k < kMaxTopk; ++k) {
         if (k >= topk) break;
-        float bs = -INFINITY;
-        int be = 0x7fffffff;
+        // a lane's candidate is always an untaken expert (or none): taken experts are skipped by
+        // their flag, not by a marker score, so -inf and NaN scores stay selectable
+        float bs = 0.0f;
+        int be = -1;
         for (int e = lane; e < E; e += 32) {
+            if (taken[e]) continue;
             const float v = score[e];
-            if (v > bs) {                             // strided scan: first (lowest) index wins ties
+            if (topk_better(v, e, bs, be)) {
                 bs = v;
                 be = e;
             }
@@ -172,13 +189,16 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) router_topk_kernel(const fl
         for (int o = 16; o > 0; o >>= 1) {
             const float os = __shfl_xor_sync(0xffffffffu, bs, o);
             const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (os > bs || (os == bs && oe < be)) {
+            if (oe >= 0 && topk_better(os, oe, bs, be)) {
                 bs = os;
                 be = oe;
             }
         }
+        // k < topk <= E experts are taken, so some lane had an untaken candidate; the clamp only
+        // keeps every index in [0, E) by construction
+        be = be < 0 ? 0 : (be >= E ? E - 1 : be);
         __syncwarp();
-        if (lane == 0) score[be] = -INFINITY;         // taken
+        if (lane == 0) taken[be] = 1;
         __syncwarp();
         pid[k] = be;
         picked[k] = sig[be];
@@ -221,7 +241,7 @@ cudaError_t launch_dense_bf16(const __nv_bfloat16* x, int T, int K, const __nv_b
     return cudaGetLastError();
 }
 
-size_t router_topk_smem_bytes(int E) { return static_cast<size_t>(2) * E * sizeof(float); }
+size_t router_topk_smem_bytes(int E) { return static_cast<size_t>(2) * E * sizeof(float) + static_cast<size_t>(E); }
 
 cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloat16* w, const float* bias, int E,
                           int topk, float routed_scale, int renorm, float* logits, int32_t* ids, float* wts,

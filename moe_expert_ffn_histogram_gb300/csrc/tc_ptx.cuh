@@ -27,16 +27,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* m, uint32_t parity, uint32_t
     return ok != 0;
 }
 
-// Bounded wait for the phase of parity `parity` of mbarrier m; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity) {
-    if (mbar_test(m, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_test(m, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
-
-// The same for a wait that is off the critical path (a whole tile long): sleeps between tries.
+// Bounded wait (about one second) for the phase of parity `parity` of mbarrier m, for a wait that
+// is off the critical path (a whole tile long): sleeps between tries. False on timeout.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* m, uint32_t parity) {
     if (mbar_test(m, parity)) return true;
     const long long t0 = clock64();
@@ -64,20 +56,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: start >> 4 (bits 0-13), leading-dimension byte offset >> 4
-// (16-29), stride-dimension byte offset >> 4 (32-45), descriptor version 1 (bits 46-47), base
-// offset 0, no swizzle (bits 61-63 = 0).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    return d;
-}
 
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzled layout that a TMA
 // load with 128-byte swizzle writes: rows of 128 bytes, 8-row groups 1024 bytes apart (stride
@@ -97,19 +75,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 template <int M, int N>
 __host__ __device__ constexpr uint32_t idesc_f16_f32() {
     return (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(M) >> 4) << 24);
-}
-constexpr uint32_t kIdesc = idesc_f16_f32<128, 128>();
-
-__device__ __forceinline__ void mma_issue_id(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
-}
-__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
-    mma_issue_id(d_tmem, adesc, bdesc, kIdesc, accumulate);
 }
 
 // D (TMEM) (+)= A (TMEM, M x 16 packed f16 pairs) x B (shared-memory descriptor), kind::f16.
@@ -176,7 +141,7 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va
     }
 }
 
-// 32 / 16 consecutive 32-bit TMEM columns of this thread's lane from registers; complete (for
+// 32 consecutive 32-bit TMEM columns of this thread's lane from registers; complete (for
 // this thread) once tmem_wait_st() returns.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
@@ -186,13 +151,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
           "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
           "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
           "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -220,22 +178,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(m)) : "memory");
-}
-
-// TMA gather: columns x.. (the map's one-row box width) of rows y0..y3, stored as four consecutive
-// box rows at dst, completing tx bytes on m.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int y0, int y1, int y2,
-                                            int y3, uint64_t* m) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-        "%4, %5, %6}], [%7];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-          "r"(smem_u32(m)) : "memory");
-}
-
-// Arrive on m once every cp.async previously issued by this thread has landed (count not raised).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* m) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(m)) : "memory");
 }
 
 }  // namespace moe

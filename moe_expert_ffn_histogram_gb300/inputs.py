@@ -298,6 +298,17 @@ class Workload:
         return self.x.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
+def to_device(wl: Workload, device) -> Workload:
+    """The same workload with its tensors (bank included) copied to `device` (no arithmetic)."""
+    def mv(obj):
+        return dataclasses.replace(obj, **{f.name: getattr(obj, f.name).to(device)
+                                          for f in dataclasses.fields(obj)
+                                          if isinstance(getattr(obj, f.name), torch.Tensor)})
+    out = mv(wl)
+    out.bank = mv(wl.bank)
+    return out
+
+
 def make_routes(kind: str, T: int, E: int, seed: int, topk: int = TOPK) -> torch.Tensor:
     if kind == "fixture":
         return fixture_routes(T, E)

@@ -45,6 +45,40 @@ def oracle_for(wl, tokens=None, ids=None, x_bits=None, limit=None, nthreads=0):
                 sub_ids[t, k] = len(used) + 10_000     # stays out of range for the sub-bank
     if not used:
         used = [0]
-    bank = wl.bank.numpy(torch.tensor(used, dtype=torch.long))
+    if used == list(range(wl.E)):
+        bank = wl.bank.numpy()                 # every expert: no gathered copy of the bank
+    else:
+        bank = wl.bank.numpy(torch.tensor(used, dtype=torch.long))
     fn = oracle.moe_fp8 if wl.fmt == "fp8" else oracle.moe_nvfp4
     return fn(xb, sub_ids, wts, bank, limit, tokens=tokens, nthreads=nthreads)
+
+
+def prefill_sample_tokens(ids, E: int, tile_rows: int = 128):
+    """Tokens whose routed pairs touch every expert that has a routed pair, and, for every expert
+    with more than one m-tile of sorted rows, the first and last row of its last (partial) m-tile
+    and the last row of its first m-tile (the grouped GEMM's tile edges). The pairs of an expert
+    are taken in the stable sorted order (ascending pair index t*topk + k)."""
+    ids = np.asarray(ids.detach().cpu().numpy() if isinstance(ids, torch.Tensor) else ids)
+    T, topk = ids.shape
+    flat = ids.reshape(-1)
+    valid = (flat >= 0) & (flat < E)
+    order = np.flatnonzero(valid)[np.argsort(flat[valid], kind="stable")]   # sorted pair indices
+    keys = flat[order]
+    starts = np.searchsorted(keys, np.arange(E), side="left")
+    ends = np.searchsorted(keys, np.arange(E), side="right")
+    chosen = set()
+    for e in range(E):
+        n = ends[e] - starts[e]
+        if n > tile_rows:
+            last0 = starts[e] + tile_rows * ((n - 1) // tile_rows)
+            for pos in (starts[e] + tile_rows - 1, last0, ends[e] - 1):
+                chosen.add(int(order[pos]) // topk)
+    need = {e for e in range(E) if ends[e] > starts[e]}
+    covered = {int(e) for t in chosen for e in ids[t] if 0 <= e < E}
+    tok_sets = [{int(e) for e in row if 0 <= e < E} for row in ids]
+    left = need - covered
+    while left:                                   # greedy cover of the experts still missing
+        best = max(range(T), key=lambda t: len(tok_sets[t] & left))
+        chosen.add(best)
+        left -= tok_sets[best]
+    return sorted(chosen)

@@ -5,6 +5,7 @@ import os
 import sys
 import types
 
+import numpy as np
 import pytest
 import torch
 
@@ -80,3 +81,42 @@ def test_cpu_baseline_fills_its_budget():
     toks = int(cb["sample"].split()[0])
     assert toks >= bench.N_ROUTE_SETS
     assert abs(cb["value"] - toks / secs) / cb["value"] < 0.1
+
+
+def test_nearest_rank_on_the_gate_binary_example():
+    # "memra-engine 0.108.0 src/bin/ep_step_fp8_gate.rs", test nearest_rank_percentiles_use_observed_samples
+    samples = [10, 20, 30, 40, 50]
+    assert bench.nearest_rank(samples, 50) == 30
+    assert bench.nearest_rank(samples, 90) == 50
+    assert bench.nearest_rank(samples, 95) == 50
+    assert bench.nearest_rank(samples, 99) == 50
+    assert bench.nearest_rank(samples, 1) == 10 and bench.nearest_rank(samples, 100) == 50
+    st = bench.step_stats_us([0.001 * v for v in (5, 1, 4, 2, 3)])
+    assert st["min"] == 1.0 and st["max"] == 5.0 and st["p50"] == 3.0 and st["mean"] == 3.0
+
+
+def _fold(values):
+    s = 0x9E3779B97F4A7C15
+    for v in np.asarray(values, dtype=np.float32).view(np.uint32):
+        s = (((s << 7) | (s >> 57)) & 0xFFFFFFFFFFFFFFFF) ^ int(v)
+    return s
+
+
+def test_output_checksum_matches_the_sequential_fold_and_is_bit_sensitive():
+    # the gate binary's test output_checksum_is_bit_sensitive_and_repeat_stable
+    vals = [0.0, -0.0, 1.0, -2.5]
+    assert bench.output_checksum(vals) == bench.output_checksum(vals)
+    assert bench.output_checksum(vals) != bench.output_checksum([0.0, 0.0, 1.0, -2.5])
+    # the closed form equals the fold taken one value at a time (lengths across the 64-bit period)
+    rng = np.random.default_rng(3)
+    for n in (0, 1, 2, 9, 10, 63, 64, 65, 1000):
+        v = rng.standard_normal(n).astype(np.float32)
+        assert bench.output_checksum(v) == _fold(v), n
+
+
+def test_graded_fraction_takes_the_larger_floor():
+    # 6.7734 GB at 6,773.4 GB/s is 1 ms; 1.93 TFLOP at 1,930 TFLOP/s is 1 ms; a 2 ms step is 0.5
+    f, floor = bench.graded_fraction(6.7734e9, 1.93e12, 2e-3, 6773.4, 1930.0)
+    assert abs(floor - 1e-3) < 1e-9 and abs(f - 0.5) < 1e-9
+    f, floor = bench.graded_fraction(13.5468e9, 1.93e12, 4e-3, 6773.4, 1930.0)   # bytes dominate
+    assert abs(floor - 2e-3) < 1e-9 and abs(f - 0.5) < 1e-9

@@ -113,3 +113,43 @@ def test_router_workspace_and_errors():
         capi.router(x, w, 9, 1.0, True)             # topk > 8
     with pytest.raises(capi.MoeError):
         capi.router(x, w, 8, 0.0, True)             # routed_scale must be > 0
+
+
+def test_router_minus_inf_bias_leaves_fewer_finite_scores_than_topk():
+    """A -inf bias masks all but topk-1 experts: the picks are those topk-1 and then the masked
+    expert of lowest index (equal -inf scores go to the lower index), exactly the oracle's
+    decision on the kernel's logits; ids stay distinct and in [0, E)."""
+    T, H, E, topk = 5, 256, 64, 8
+    x, w, _ = _make(T, H, E, seed=21, bias=False)
+    b = torch.full((E,), float("-inf"), dtype=torch.float32, device=DEV)
+    keep = torch.tensor([5, 17, 33, 40, 41, 50, 63], device=DEV)
+    b[keep] = 0.0
+    ids, wts, logits = capi.router(x, w, topk, 1.0, True, bias=b, want_logits=True)
+    torch.cuda.synchronize()
+    g_ids = ids.cpu().numpy()
+    o_ids, o_w = oracle.router_topk(logits.double().cpu().numpy(), b.double().cpu().numpy(), topk, 1.0, True)
+    assert g_ids.tolist() == o_ids.tolist()
+    for t in range(T):
+        assert sorted(g_ids[t, :topk - 1].tolist()) == keep.cpu().tolist()
+        assert g_ids[t, topk - 1] == 0
+    assert np.allclose(wts.double().cpu().numpy(), o_w, rtol=2e-6, atol=1e-7)
+
+
+def test_router_nan_logits_give_valid_distinct_ids():
+    """NaN logits (a NaN router row, and a token whose x is NaN) never produce an index outside
+    [0, E) or a repeated pick; experts with a number for a score come before NaN ones."""
+    T, H, E, topk = 4, 256, 32, 8
+    x, w, b = _make(T, H, E, seed=22)
+    w = w.clone()
+    w[[2, 9, 30]] = float("nan")                 # three experts score NaN for every token
+    x = x.clone()
+    x[3] = float("nan")                          # token 3 scores NaN for every expert
+    ids, wts, _ = capi.router(x, w, topk, 1.0, True, bias=b)
+    torch.cuda.synchronize()
+    g = ids.cpu().numpy()
+    assert ((g >= 0) & (g < E)).all()
+    for t in range(T):
+        assert len(set(g[t].tolist())) == topk
+    for t in range(3):                           # finite scores exist for 29 experts: NaN ones lose
+        assert not set(g[t].tolist()) & {2, 9, 30}
+    assert g[3].tolist() == list(range(topk))    # all NaN: by index

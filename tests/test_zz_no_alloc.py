@@ -49,8 +49,12 @@ def entry():
     return _entry()
 
 
-@pytest.mark.parametrize("T", [1, 5])
+@pytest.mark.parametrize("T", [1, 5, 17])
 def test_noalloc_matches_workspace_entry_point_two_calls(entry, T):
+    """Two calls in a row with different inputs; each is bit-identical to moe_fp8_forward with a
+    caller workspace (the same kernels on the same inputs). T = 17 runs three sweeps of <= 8
+    tokens that reuse the scratch regions, the barrier word included, in stream order."""
+    assert capi.workspace_bytes(T, 1024, 512, 16, 8, capi.FMT_FP8) <= SCRATCH_BYTES
     bank = inputs.make_fp8_bank(16, 1024, 512, seed=404, device=DEV)
     for call in range(2):                      # two calls in a row, different inputs
         wl = inputs.make_custom("fp8", T, 1024, 512, 16, seed=500 + call, device=DEV)
@@ -60,6 +64,7 @@ def test_noalloc_matches_workspace_entry_point_two_calls(entry, T):
         err = torch.zeros(1, dtype=torch.int32, device=DEV)
         assert _noalloc(entry, wl, out, err) == 0
         torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"noalloc T={T} call {call}"
         check_close(bf16_to_f64(out), bf16_to_f64(ref), f"noalloc T={T} call {call}")
         assert int(err.item()) == 0
 

@@ -306,18 +306,26 @@ def output_checksum(values) -> int:
     starting from 0x9e3779b97f4a7c15 (the gate binary's `output_checksum`, "memra-engine 0.108.0
     src/bin/ep_step_fp8_gate.rs", benchmark harness). bf16 results are widened to fp32 first.
     The fold is linear over XOR, so it is evaluated in closed form: v_i enters rotated by
-    7 * (n - 1 - i) and the start value by 7 * n."""
+    7 * (n - 1 - i) mod 64, which depends only on i mod 64, so each residue class is XOR-reduced
+    first and the 64 partial results are rotated once each; the start value enters rotated by
+    7 * n mod 64."""
     a = np.ascontiguousarray(np.asarray(values, dtype=np.float32)).reshape(-1)
     n = a.size
     bits = a.view(np.uint32).astype(np.uint64)
-    rot = ((7 * (n - 1 - np.arange(n, dtype=np.int64))) % 64).astype(np.uint64)
-    back = (np.uint64(64) - rot) % np.uint64(64)
-    rotated = (bits << rot) | np.where(rot == 0, np.uint64(0), bits >> back)
-    acc = int(np.bitwise_xor.reduce(rotated)) if n else 0
-    r0 = (7 * n) % 64
-    s0 = 0x9E3779B97F4A7C15
-    s0 = ((s0 << r0) | (s0 >> (64 - r0))) & 0xFFFFFFFFFFFFFFFF if r0 else s0
-    return s0 ^ acc
+    pad = (-n) % 64
+    if pad:
+        bits = np.concatenate([bits, np.zeros(pad, dtype=np.uint64)])
+    cols = np.bitwise_xor.reduce(bits.reshape(-1, 64), axis=0) if bits.size else np.zeros(64, np.uint64)
+    mask = (1 << 64) - 1
+
+    def rotl(v, r):
+        r %= 64
+        return ((v << r) | (v >> (64 - r))) & mask if r else v
+
+    acc = rotl(0x9E3779B97F4A7C15, 7 * n)
+    for j in range(64):
+        acc ^= rotl(int(cols[j]), 7 * (n - 1 - j))
+    return acc
 
 
 def graded_fraction(alg_bytes, flops, seconds, hbm_gbs, bf16_tflops):

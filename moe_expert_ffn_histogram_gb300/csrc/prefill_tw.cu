@@ -42,6 +42,7 @@
 
 #include "prefill.cuh"
 #include "tc_ptx.cuh"
+#include "tma_map.cuh"
 
 
 namespace moe {
@@ -223,8 +224,8 @@ __global__ void __launch_bounds__(kTwThreads, 1)
         // NM = 1. Raw rows: FP8 128 bytes in 16-byte chunks, 128-byte swizzle (chunk ^ row % 8);
         // NVFP4 64 bytes of packed codes, 64-byte swizzle (chunk ^ (row / 2) % 4). Eight
         // consecutive lanes read eight consecutive rows of one chunk, which the swizzle places in
-        // eight distinct bank groups. The raw boxes are released once the last piece is in
-        // registers; the TMEM slot is waited for only before the first store.
+        // eight distinct bank groups. The raw boxes are released once the last piece has been
+        // converted; the TMEM slot is waited for only before the first store.
         const int cw = warp - kTwConvWarp0, qd = warp & 3, part = cw / 4;
         const int rrow = (NM == 2 ? part * 128 : 0) + 32 * qd + lane;       // raw row of this thread
         const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
@@ -302,15 +303,11 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 const uint32_t ta = tmem + lane_off + Cfg::kA0 + s * Cfg::kACols + (NM == 2 ? part * Cfg::kMCols : part * 32);
 #pragma unroll
                 for (int pc = 0; pc < kPieces; ++pc) {
-                    // the piece's chunks; after the last piece's loads the raw boxes are released
+                    // the piece's chunks
                     uint4 wr[kPieceChunks];
 #pragma unroll
                     for (int c = 0; c < kPieceChunks; ++c)
                         wr[c] = lds128(raw + (((c0 + pc * kPieceChunks + c) ^ sw) << 4));
-                    if (pc == kPieces - 1) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&rempty[r]);
-                    }
                     uint32_t h[32];
                     if constexpr (FMT == 0) {
                         const uint32_t sc2 = tbl[kt];
@@ -343,6 +340,13 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                                 for (int b = 0; b < 4; ++b) h[16 * c + 4 * i + b] = hmul2(qq[b], sf2);
                             }
                         }
+                    }
+                    // the raw boxes are released once the last piece has been converted (the
+                    // conversion consumes the loaded registers): a release right after the
+                    // shared-memory loads can let the next box land before they have returned
+                    if (pc == kPieces - 1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&rempty[r]);
                     }
                     if (pc == 0 && !__all_sync(0xffffffffu, us == 0 || tw_wait(&sempty[s], (us - 1) & 1u))) {
                         ok = false;
@@ -572,30 +576,10 @@ __global__ void __launch_bounds__(kTwThreads, 1)
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 tw_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            f = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }();
-    return fn;
-}
-
 // 2-D map over a row-major [rows][inner] matrix of elem-byte elements, box box_inner x 128.
 bool tw_map(CUtensorMap* m, CUtensorMapDataType dt, int elem, const void* base, uint64_t inner, uint64_t rows,
             uint32_t box_inner, CUtensorMapSwizzle sw) {
-    auto enc = tw_encoder();
-    if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem)};
-    const cuuint32_t box[2] = {box_inner, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_map_2d(m, dt, elem, base, inner, rows, box_inner, 128, sw);
 }
 
 template <int KIND, int NM, int DB, int FMT>

@@ -27,6 +27,12 @@ using namespace moe;
 #ifndef MOE_FORWARD_FUSED
 #define MOE_FORWARD_FUSED 1
 #endif
+#ifndef MOE_FP4_TOKEN
+#define MOE_FP4_TOKEN 1
+#endif
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
 #ifndef MOE_FORCE_FUSED
 #define MOE_FORCE_FUSED 0
 #endif
@@ -163,6 +169,8 @@ int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, co
     a.act = w.at<__half>(w.L.act);
     a.act_scale = w.at<float>(w.L.act_scale);
     a.err = err;
+    if (MOE_FP4_TOKEN && FMT == 1 && rows == 1)   // one NVFP4 token: the lean single-token kernel
+        return cuda_status(launch_fp4_token_gate_up(a, topk, s));
     const int ngroups = rows * topk;     // implicit: topk slots; table: at most one per pair
     const int cap = rows == 1 ? 1 : group_cap(rows, topk);
     // NVFP4, one token: prefetch the call's whole weight set into L2 when it fits (<= 96 MB,
@@ -201,6 +209,8 @@ int stage_down(int rows, int H, int I, int E, int topk, const int32_t* ids, cons
     a.out = reinterpret_cast<__nv_bfloat16*>(out);
     a.shared = reinterpret_cast<const __nv_bfloat16*>(shared);
     a.residual = reinterpret_cast<const __nv_bfloat16*>(residual);
+    if (MOE_FP4_TOKEN && FMT == 1 && rows == 1)
+        return cuda_status(launch_fp4_token_down(a, MOE_PDL != 0, s));
     return cuda_status(launch_down_combine<FMT>(a, s));
 }
 

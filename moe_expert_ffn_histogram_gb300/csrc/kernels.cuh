@@ -58,6 +58,11 @@ template <int FMT> cudaError_t launch_down_combine(const DownArgs& a, cudaStream
 size_t gate_up_smem_bytes(int H, int max_cols);
 size_t down_smem_bytes(int T, int topk);
 
+// Single-token NVFP4 decode (decode_fp4.cu): the same workspace format as launch_gate_up /
+// launch_down_combine for one token, fewer instructions per weight byte.
+cudaError_t launch_fp4_token_gate_up(const GateUpArgs& a, int topk, cudaStream_t stream);
+cudaError_t launch_fp4_token_down(const DownArgs& a, bool pdl, cudaStream_t stream);
+
 // The whole forward of one sub-batch in one cooperative launch (fused.cu); `barrier` is a
 // workspace word, zeroed by the launcher with a memset on `stream`.
 template <int FMT> cudaError_t launch_fused_forward(const GateUpArgs& ga, const DownArgs& da,

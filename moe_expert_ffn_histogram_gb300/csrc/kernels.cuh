@@ -75,7 +75,7 @@ void set_test_barrier_timeout(bool on);
 // Wide tier (prefill.cu): workspace layout and the launch sequence of the grouped-GEMM path.
 struct PrefillLayout {
     size_t counts, offsets, sorted_pair, pair_to_sorted, tiles, tile_e, tile_r0, tile_first, tile_cnt;
-    size_t x16, xinv, amax, a16, ainv, f32, plan_blk, total;
+    size_t x16, xinv, amax, a16, ainv, f32, tmax, yexp, plan_blk, total;
 };
 PrefillLayout prefill_layout(int T, int H, int I, int E, int topk);
 // Weights of the three projections for the prefill tier: FP8 codes + fp32 block scales, or

@@ -15,7 +15,8 @@
 //                            SwiGLU in the epilogue -> a (prefill_tw.cu, the TMEM core)
 //   prefill_act_prep         a (fp32) -> a16 (f16, one power-of-two range scale per sorted row),
 //                            only when no clamp limit bounds a (with one the GEMM writes a16)
-//   down grouped GEMM        per tile of 128 sorted rows x 128 output rows: y (fp32)
+//   down grouped GEMM        per tile of 128 sorted rows x 128 output rows: y, stored in f16 times
+//                            a power of two per (sorted row, 128-row block) from a bound on |y|
 //   prefill_combine          out[t] = sum over slots k in order of w[t,k] * y[pair_to_sorted], bf16
 //
 // Weights are dequantised by the GEMM's converter warps: E4M3 -> f16 exactly, times the block
@@ -163,15 +164,18 @@ __global__ void __launch_bounds__(256) prefill_act_prep_kernel(const float* __re
 
 // out[t][j] = bf16( sum_{k in slot order} w[t,k] * y[pair_to_sorted[t*topk+k]][j] ), a separate
 // rounded multiply and add per term (ep_step_fp8_gate.rs, `combine_down_rows_host`; the indexed
-// twin of forward.rs's `glm5next_moe_combine_indexed`). One block per token.
-__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ y,
+// twin of forward.rs's `glm5next_moe_combine_indexed`). y arrives as f16 y * 2^g with g per sorted
+// row and 128-row output block (yexp); y16 * 2^-g is exact in fp32. One block per token, 8
+// consecutive outputs per thread and step (16-byte loads).
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const __half* __restrict__ y16,
+                                                              const int8_t* __restrict__ yexp,
                                                               const int32_t* __restrict__ pair_to_sorted,
                                                               const float* __restrict__ wts,
                                                               int topk, int H,
                                                               __nv_bfloat16* __restrict__ out,
                                                               const __nv_bfloat16* __restrict__ shared,
                                                               const __nv_bfloat16* __restrict__ residual) {
-    const int t = blockIdx.x;
+    const int t = blockIdx.x, nb = H / 128;
     int rows[kMaxTopk];
     float w[kMaxTopk];
 #pragma unroll
@@ -179,28 +183,47 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
         rows[k] = k < topk ? pair_to_sorted[t * topk + k] : -1;
         w[k] = k < topk ? wts[t * topk + k] : 0.0f;
     }
-    for (int j = threadIdx.x * 4; j < H; j += 256 * 4) {
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = threadIdx.x * 8; j < H; j += 256 * 8) {
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < kMaxTopk; ++k) {
             if (rows[k] < 0) continue;
-            const float4 v = *reinterpret_cast<const float4*>(y + static_cast<size_t>(rows[k]) * H + j);
-            s[0] = __fadd_rn(s[0], __fmul_rn(w[k], v.x));
-            s[1] = __fadd_rn(s[1], __fmul_rn(w[k], v.y));
-            s[2] = __fadd_rn(s[2], __fmul_rn(w[k], v.z));
-            s[3] = __fadd_rn(s[3], __fmul_rn(w[k], v.w));
+            const size_t r = static_cast<size_t>(rows[k]);
+            const uint4 v = __ldcs(reinterpret_cast<const uint4*>(y16 + r * H + j));
+            const float unscale = __int_as_float((127 - yexp[r * nb + (j >> 7)]) << 23);   // 2^-g
+            const uint32_t hv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv[q]));
+                s[2 * q] = __fadd_rn(s[2 * q], __fmul_rn(w[k], f.x * unscale));
+                s[2 * q + 1] = __fadd_rn(s[2 * q + 1], __fmul_rn(w[k], f.y * unscale));
+            }
         }
         const size_t oj = static_cast<size_t>(t) * H + j;
+        if (shared != nullptr || residual != nullptr) {   // layer epilogue: (routed + shared) + residual
+            uint4 sh = make_uint4(0, 0, 0, 0), rs = make_uint4(0, 0, 0, 0);
+            if (shared != nullptr) sh = *reinterpret_cast<const uint4*>(shared + oj);
+            if (residual != nullptr) rs = *reinterpret_cast<const uint4*>(residual + oj);
+            const uint32_t shv[4] = {sh.x, sh.y, sh.z, sh.w}, rsv[4] = {rs.x, rs.y, rs.z, rs.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {                 // layer epilogue: (routed + shared) + residual
-            if (shared != nullptr) s[q] = __fadd_rn(s[q], __bfloat162float(shared[oj + q]));
-            if (residual != nullptr) s[q] = __fadd_rn(s[q], __bfloat162float(residual[oj + q]));
+            for (int q = 0; q < 4; ++q) {
+                if (shared != nullptr) {
+                    s[2 * q] = __fadd_rn(s[2 * q], __uint_as_float(shv[q] << 16));
+                    s[2 * q + 1] = __fadd_rn(s[2 * q + 1], __uint_as_float(shv[q] & 0xFFFF0000u));
+                }
+                if (residual != nullptr) {
+                    s[2 * q] = __fadd_rn(s[2 * q], __uint_as_float(rsv[q] << 16));
+                    s[2 * q + 1] = __fadd_rn(s[2 * q + 1], __uint_as_float(rsv[q] & 0xFFFF0000u));
+                }
+            }
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(s[0], s[1]), hi = __floats2bfloat162_rn(s[2], s[3]);
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&lo);
-        o.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(out + static_cast<size_t>(t) * H + j) = o;
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(s[2 * q], s[2 * q + 1]);
+            o[q] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        *reinterpret_cast<uint4*>(out + oj) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -231,7 +254,9 @@ PrefillLayout prefill_layout(int T, int H, int I, int E, int topk) {
     L.amax = take(P * 4);
     L.a16 = take(P * static_cast<size_t>(I) * 2);
     L.ainv = take(P * 4);
-    L.f32 = take(P * static_cast<size_t>(H > I ? H : I) * 4);   // a (fp32), later y
+    L.f32 = take(P * static_cast<size_t>(H > I ? H : I) * 4);   // a (fp32), later y (f16)
+    L.tmax = take(mtiles * 4);                                 // max |a| per m-tile
+    L.yexp = take(P * static_cast<size_t>(H / prefill::kBN));   // y's power of two per row and block
     L.plan_blk = take(route_plan_wide_ws_bytes(static_cast<int>(P), E));
     L.total = o;
     return L;
@@ -271,8 +296,17 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     // a finite clamp limit L <= 255 bounds |a| = |silu(min(g, L)) * clamp(u, -L, L)| by L^2, which
     // f16 holds without a range scale: the TMEM core then writes a in f16 itself
     const bool a16_direct = std::isfinite(limit) && limit <= kA16DirectLimit;
+    // the direct f16 activations carry one power of two 2^s with L^2 * 2^s < 2^15, so that small
+    // activations stay clear of f16's subnormal range
+    int l2e = 0;
+    if (a16_direct) std::frexp(static_cast<double>(limit) * limit, &l2e);
+    const int a16_s = a16_direct && limit > 0.0f ? 15 - l2e : 0;
+    // max |a| per sorted row (range-scaled activations: their scale, and y's f16 factor) or per
+    // m-tile (f16 activations under the clamp: y's f16 factor)
+    uint32_t* tmax = reinterpret_cast<uint32_t*>(ws + L.tmax);
     if (!a16_direct && (st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess)
         return st;
+    if (a16_direct && (st = cudaMemsetAsync(tmax, 0, L.yexp - L.tmax, stream)) != cudaSuccess) return st;
 
     float* f32 = reinterpret_cast<float*>(ws + L.f32);
     PrefillGemmArgs gu{};
@@ -296,7 +330,9 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     gu.limit = limit;
     gu.out = f32;
     gu.amax = amax;
+    gu.tmax = tmax;
     gu.out16 = a16_direct ? reinterpret_cast<__half*>(ws + L.a16) : nullptr;
+    gu.a16_scale = std::ldexp(1.0f, a16_s);
     gu.out_ld = I;
     gu.err = err;
     gu.a_rows = P;
@@ -322,6 +358,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     dn.n_tiles = H / prefill::kBN;
     dn.a = a16;
     dn.a_inv = a16_direct ? nullptr : ainv;
+    dn.a16_scale = std::ldexp(1.0f, -a16_s);
     dn.out16 = nullptr;
     dn.w0 = wd;
     dn.s0 = sd;
@@ -332,16 +369,18 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     dn.sf1 = wt.sfd;
     dn.s2_0 = wt.s2d;
     dn.s2_1 = wt.s2d;
-    dn.out = f32;
-    dn.amax = nullptr;
+    dn.out = nullptr;
+    dn.y16 = reinterpret_cast<__half*>(f32);
+    dn.yexp = reinterpret_cast<int8_t*>(ws + L.yexp);
+    dn.amax = amax;
     dn.out_ld = H;
     dn.a_rows = P;
     stage_mark(stream, "down_gemm");
     if ((st = launch_prefill_gemm_tw(1, dn, H, stream)) != cudaSuccess) return st;
 
     stage_mark(stream, "combine");
-    prefill_combine_kernel<<<T, 256, 0, stream>>>(f32, I32(L.pair_to_sorted), wts, topk, H, out, shared,
-                                                  residual);
+    prefill_combine_kernel<<<T, 256, 0, stream>>>(dn.y16, dn.yexp, I32(L.pair_to_sorted), wts, topk, H, out,
+                                                  shared, residual);
     return cudaGetLastError();
 }
 

@@ -33,12 +33,20 @@ struct PrefillGemmArgs {
     int wrows;                   // rows of one expert's weight matrix (I for gate/up, H for down)
     float limit;
     // outputs
-    float* out;                  // KIND 0: a32 [P][I]; KIND 1: y [P][H]
-    uint32_t* amax;              // KIND 0: per sorted row max |a| (float bits), zeroed before
-    // KIND 0, TMEM core: when set, a goes straight to f16 here ([P][I], no range scale: a finite
-    // clamp limit L <= 255 bounds |a| by L^2 < 65504), and out / amax are not used; KIND 1 then
-    // runs with a_inv == nullptr (scale 1)
+    float* out;                  // KIND 0: a32 [P][I]
+    // KIND 1: y [P][H] in f16 as y * 2^g, g = yexp[row][n-tile] chosen per sorted row and 128-row
+    // output block from a bound on |y| (so that |y| * 2^g < 2^15); the combine multiplies by 2^-g
+    __half* y16;
+    int8_t* yexp;                // [P][H / 128]
+    uint32_t* amax;              // per sorted row max |a| (float bits) of the range-scaled path:
+                                 // KIND 0 writes it (zeroed before), KIND 1 reads it for y's factor
+    uint32_t* tmax;              // per m-tile max |a| (float bits) of the f16 path (out16): the same
+    // KIND 0, TMEM core: when set, a goes straight to f16 here ([P][I]) as a * a16_scale, one power
+    // of two for all rows (a finite clamp limit L <= 255 bounds |a| by L^2, and L^2 * a16_scale <
+    // 2^15), out and amax are not used (tmax is); KIND 1 then runs with a_inv == nullptr and
+    // a16_scale holding the inverse
     __half* out16;
+    float a16_scale;
     int out_ld;                  // I (KIND 0) or H (KIND 1)
     int32_t* err;                // optional error word (bit 1: a bounded wait gave up)
     int a_rows;                  // rows of the A matrix: T (KIND 0) or P (KIND 1)
@@ -78,6 +86,28 @@ __device__ __forceinline__ float weight_prescale(const float* srow, int KB, uint
             tbl[kb] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&h)) * 0x10001u;
         }
     return inv;
+}
+
+// sum over the KB 128-wide K blocks of |scale| of one (expert, 128-row weight block) scale row, the
+// same value in every lane (a fixed shuffle tree). One warp.
+__device__ __forceinline__ float block_scale_abs_sum(const float* srow, int KB) {
+    const int lane = threadIdx.x & 31;
+    float v = 0.0f;
+    for (int kb = lane; kb < KB; kb += 32) v += fabsf(srow[kb]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exponent g with a * w * 2^g < 2^15 for positive finite a and w (0 when either is zero or not
+// finite), clamped to [-100, 100]: with m = a * w < 2^(ea + ew), g = 15 - ea - ew.
+__device__ __forceinline__ int pow2_bound_exponent(float a, float w) {
+    if (!(a > 0.0f) || !(w > 0.0f) || !isfinite(a) || !isfinite(w)) return 0;
+    int ea, ew;
+    frexpf(a, &ea);
+    frexpf(w, &ew);
+    const int g = 15 - ea - ew;
+    return g < -100 ? -100 : (g > 100 ? 100 : g);
 }
 
 // The same table from scales already in registers: lane holds kb = lane (v0) and lane + 32 (v1),

@@ -360,6 +360,22 @@ def test_prefill_activation_paths_at_the_limit_bound(limit):
     check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"prefill limit {limit}")
 
 
+@pytest.mark.parametrize("fmt,x_scale,limit", [("fp8", 3e-3, 7.0), ("fp8", 2e3, float("inf")),
+                                               ("fp8", 3e-3, float("inf")), ("nvfp4", 3e-3, 7.0),
+                                               ("nvfp4", 2e3, float("inf"))])
+def test_prefill_f16_scaling_across_magnitudes(fmt, x_scale, limit):
+    """The grouped tier keeps its activations and the down GEMM's output y in f16 times powers of
+    two (a fixed one for the clamped activations, one per sorted row and 128-row output block for
+    y, from a bound on |y|): tiny inputs stay clear of f16's subnormal range and large ones (y far
+    above 65504 without the clamp) below its largest value, both against the oracle."""
+    H, I = (256, 256) if fmt == "fp8" else (512, 256)
+    wl = inputs.make_custom(fmt, 40, H, I, 10, seed=970, device=DEV, x_scale=x_scale, limit=limit)
+    ref = oracle_for(wl)["out"]
+    if x_scale > 1.0:
+        assert np.abs(ref).max() > 65504.0        # y itself leaves f16's range
+    check_close(bf16_to_f64(run(wl)), ref, f"{fmt} prefill x*{x_scale} limit {limit}")
+
+
 # ---- bounded waits and buffer bounds -----------------------------------------------------------------
 
 @pytest.mark.parametrize("fmt,T", [("fp8", 4), ("nvfp4", 7)])

@@ -30,9 +30,6 @@ using namespace moe;
 #ifndef MOE_FP4_TOKEN
 #define MOE_FP4_TOKEN 1
 #endif
-#ifndef MOE_PDL
-#define MOE_PDL 1
-#endif
 #ifndef MOE_FORCE_FUSED
 #define MOE_FORCE_FUSED 0
 #endif

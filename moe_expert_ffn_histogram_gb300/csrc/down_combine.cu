@@ -2,10 +2,7 @@
 // rows. The work item itself is down_item (gemv_items.cuh).
 #include "gemv_items.cuh"
 
-// Launch as a programmatic dependent of the preceding gate/up kernel (see down_item).
-#ifndef MOE_PDL
-#define MOE_PDL 1
-#endif
+// Launched as a programmatic dependent of the preceding gate/up kernel (see down_item).
 
 namespace moe {
 

@@ -156,6 +156,13 @@ __device__ __forceinline__ void prefetch_l2_range(const uint8_t* p, size_t bytes
     }
 }
 
+// Programmatic dependent launch (1: on): a dependent kernel is launched while the one before it
+// on the stream still runs, does its setup, and waits in griddepcontrol.wait for that grid's
+// completion before it reads what the grid wrote.
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
+
 // Programmatic dependent launch: let the next kernel on the stream start launching, and (in that
 // kernel) wait until every grid it depends on has completed and its writes are visible.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(256) prefill_x_prep_kernel(const __nv_bfloat16
                                                              const int32_t* __restrict__ pair_to_sorted,
                                                              int topk) {
     __shared__ float red[8];
+    pdl_launch_dependents();                           // the gate/up GEMM may start its setup
     const int t = blockIdx.x, tid = threadIdx.x;
     const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
     const int nv = H / 8;
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const __half* __re
                                                               const __nv_bfloat16* __restrict__ shared,
                                                               const __nv_bfloat16* __restrict__ residual) {
     const int t = blockIdx.x, nb = H / 128;
+    pdl_wait();                                        // y of the down GEMM (programmatic dependent)
     int rows[kMaxTopk];
     float w[kMaxTopk];
 #pragma unroll
@@ -286,12 +288,6 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
                                                  I32(L.tile_e), I32(L.tile_r0), I32(L.tile_first),
                                                  I32(L.tile_cnt));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
-    __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
-    float* xinv = reinterpret_cast<float*>(ws + L.xinv);
-    stage_mark(stream, "x_prep");
-    prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv,
-                                                  I32(L.pair_to_sorted), topk);
-    if ((st = cudaGetLastError()) != cudaSuccess) return st;
     uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
     // a finite clamp limit L <= 255 bounds |a| = |silu(min(g, L)) * clamp(u, -L, L)| by L^2, which
     // f16 holds without a range scale: the TMEM core then writes a in f16 itself
@@ -302,11 +298,18 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     if (a16_direct) std::frexp(static_cast<double>(limit) * limit, &l2e);
     const int a16_s = a16_direct && limit > 0.0f ? 15 - l2e : 0;
     // max |a| per sorted row (range-scaled activations: their scale, and y's f16 factor) or per
-    // m-tile (f16 activations under the clamp: y's f16 factor)
+    // m-tile (f16 activations under the clamp: y's f16 factor); zeroed before x prep, so that the
+    // gate/up GEMM follows x prep directly (programmatic dependent launch)
     uint32_t* tmax = reinterpret_cast<uint32_t*>(ws + L.tmax);
     if (!a16_direct && (st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess)
         return st;
     if (a16_direct && (st = cudaMemsetAsync(tmax, 0, L.yexp - L.tmax, stream)) != cudaSuccess) return st;
+    __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
+    float* xinv = reinterpret_cast<float*>(ws + L.xinv);
+    stage_mark(stream, "x_prep");
+    prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv,
+                                                  I32(L.pair_to_sorted), topk);
+    if ((st = cudaGetLastError()) != cudaSuccess) return st;
 
     float* f32 = reinterpret_cast<float*>(ws + L.f32);
     PrefillGemmArgs gu{};
@@ -379,8 +382,19 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     if ((st = launch_prefill_gemm_tw(1, dn, H, stream)) != cudaSuccess) return st;
 
     stage_mark(stream, "combine");
-    prefill_combine_kernel<<<T, 256, 0, stream>>>(dn.y16, dn.yexp, I32(L.pair_to_sorted), wts, topk, H, out,
-                                                  shared, residual);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(T);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((st = cudaLaunchKernelEx(&cfg, prefill_combine_kernel, static_cast<const __half*>(dn.y16),
+                                 static_cast<const int8_t*>(dn.yexp), static_cast<const int32_t*>(I32(L.pair_to_sorted)),
+                                 wts, topk, H, out, shared, residual)) != cudaSuccess)
+        return st;
     return cudaGetLastError();
 }
 

@@ -170,6 +170,10 @@ __global__ void __launch_bounds__(kTwThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
+    // launched as a programmatic dependent: the setup above overlaps the previous kernel's tail;
+    // nothing it wrote is read before this wait
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp < kTwConvWarp0) {
         // ---------------- producers ----------------
@@ -473,8 +477,11 @@ __global__ void __launch_bounds__(kTwThreads, 1)
         // Warp w reads TMEM lanes 32*(w%4)..+31 (lane = weight row f of the tile's slab) and token
         // columns 64*h..+63, h = (w - 12) / 4. Each store instruction writes one token row's 32
         // consecutive features (128 contiguous bytes).
-        __shared__ float xs_s[kTwEpiWarps][64];            // per epilogue warp: its tokens' scales
-        __shared__ float ys_s[kTwEpiWarps][64];            // down: its rows' f16 output factors 2^g
+        // per epilogue warp and column: the factor of the accumulator - the token's or row's
+        // activation scale times the weight block's inverse prescale (gate/up: gate in xs_s, up
+        // in ys_s; down: in ys_s, with y's power of two for f16)
+        __shared__ float xs_s[kTwEpiWarps][64];
+        __shared__ float ys_s[kTwEpiWarps][64];
         const int ew = warp - kTwEpiWarp0, qd = warp & 3, cbase = 64 * (ew / 4);
         const int f = 32 * qd + lane;
         const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
@@ -516,9 +523,17 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                     const float arow = p.a_inv != nullptr ? __uint_as_float(p.amax[r0 + min(cbase + t, rows - 1)])
                                                           : __uint_as_float(p.tmax[mt]);
                     const int g = pow2_bound_exponent(arow, wsum);
-                    ys_s[ew][t] = __int_as_float((127 + g) << 23);
+                    ys_s[ew][t] = (xs_s[ew][t] * winv0) * __int_as_float((127 + g) << 23);
                     if (qd == 0 && cbase + t < rows)
                         p.yexp[static_cast<size_t>(r0 + cbase + t) * p.n_tiles + nt] = static_cast<int8_t>(g);
+                }
+            }
+            if constexpr (KIND == 0) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int t = 32 * i + lane;
+                    ys_s[ew][t] = xs_s[ew][t] * winv1;
+                    xs_s[ew][t] = xs_s[ew][t] * winv0;
                 }
             }
             __syncwarp();
@@ -544,13 +559,12 @@ __global__ void __launch_bounds__(kTwThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int t = c0 + j;
-                        const float xs = xs_s[ew][t];
                         // the clamped SwiGLU with silu(g) = g/2 * (1 + tanh(g/2)): one SFU operation
                         // (tanh.approx, about 2^-11 absolute error) instead of an exponential and a
                         // divide - the epilogue holds the single accumulator, so its length stalls
                         // the MMA (measured: gate/up GEMM 2,164 -> 2,134 us)
-                        const float gg = fminf(gv[j] * xs * winv0, p.limit);
-                        const float uu = fminf(fmaxf(uv[j] * xs * winv1, -p.limit), p.limit);
+                        const float gg = fminf(gv[j] * xs_s[ew][t], p.limit);
+                        const float uu = fminf(fmaxf(uv[j] * ys_s[ew][t], -p.limit), p.limit);
                         const float hg = 0.5f * gg;
                         const float h = hg * (1.0f + tanh_approx(hg)) * uu;
                         if (dst16 != nullptr) {                // bounded by the clamp: f16 as is
@@ -572,8 +586,7 @@ __global__ void __launch_bounds__(kTwThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int t = c0 + j;
-                        const float y = yv[j] * xs_s[ew][t] * winv0;
-                        if (t < vrows) dsty[static_cast<size_t>(t) * p.out_ld] = __float2half_rn(y * ys_s[ew][t]);
+                        if (t < vrows) dsty[static_cast<size_t>(t) * p.out_ld] = __float2half_rn(yv[j] * ys_s[ew][t]);
                     }
                 }
             }
@@ -630,7 +643,18 @@ cudaError_t launch_tw(const PrefillGemmArgs& q, const CUtensorMap& a, const CUte
     cudaError_t st = cudaFuncSetAttribute(prefill_tw_gemm_kernel<KIND, NM, DB, FMT>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (st != cudaSuccess) return st;
-    prefill_tw_gemm_kernel<KIND, NM, DB, FMT><<<grid, kTwThreads, Cfg::kSmem, stream>>>(q, a, w0, w1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTwThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((st = cudaLaunchKernelEx(&cfg, prefill_tw_gemm_kernel<KIND, NM, DB, FMT>, q, a, w0, w1)) != cudaSuccess)
+        return st;
     return cudaGetLastError();
 }
 

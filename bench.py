@@ -384,13 +384,21 @@ def measure_workload(name, args, dev, bank, world, peak, peak_kind, tpeak, want_
           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
+    if args.profile_range:            # a profiler started with its capture off records from here
+        torch.cuda.cudart().cudaProfilerStart()
     for i in range(args.steps):
         flush.zero_()
         hold_stream()
+        if args.profile_range:
+            torch.cuda.nvtx.range_push(f"{name}/step")
         ev[i][0].record(stream)
         fwd(sets[i % N_ROUTE_SETS], outs[i])
         ev[i][1].record(stream)
+        if args.profile_range:
+            torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
+    if args.profile_range:
+        torch.cuda.cudart().cudaProfilerStop()
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     clk = clocks.stop()
@@ -740,6 +748,11 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--profile-range", action="store_true",
+                    help="bracket each workload's timed steps with cudaProfilerStart/Stop and one "
+                         "NVTX range per step ('<workload>/step'; the library adds a range per "
+                         "forward and per stage), for `ncu --profile-from-start off` or "
+                         "`--nvtx --nvtx-include`")
     ap.add_argument("--lib", default=None, help="path of an alternative build of the library")
     ap.add_argument("--bank-experts", type=int, default=None,
                     help="use only the first N experts of the bank (small profiling captures)")

@@ -276,7 +276,7 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
             const uint16_t* residual = nullptr) {
     int rc = check_sizes(T, H, I, E, topk);
     if (rc) return rc;
-    StageScope timing(s);
+    StageScope timing(s, FMT == 0 ? "moe_fp8_forward" : "moe_nvfp4_forward");
     if (uses_prefill(T, H, I, E, FMT)) {
         if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
         const PrefillLayout L = prefill_layout(T, H, I, E, topk);

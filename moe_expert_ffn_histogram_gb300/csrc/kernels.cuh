@@ -109,17 +109,75 @@ cudaError_t launch_shared_expert(const __nv_bfloat16* x, int T, int H, int S, co
                                  const __nv_bfloat16* wu, const __nv_bfloat16* wd, float limit,
                                  __nv_bfloat16* out, uint8_t* ws, int sms, cudaStream_t stream);
 
+// The grouped tier's m-tile list (the tiles of rows_per_tile sorted rows of each expert, in
+// ascending expert order): tiles[0] = number of m-tiles; tile_e[i], tile_r0[i] = expert and first
+// sorted row of tile i; tile_first[i], tile_cnt[i] = first m-tile and number of m-tiles of that
+// expert. Null tiles: no list.
+struct TileList {
+    int32_t* tiles;
+    int32_t* tile_e;
+    int32_t* tile_r0;
+    int32_t* tile_first;
+    int32_t* tile_cnt;
+    int rows_per_tile;
+};
+
+// Builds the list from per-expert counts and offsets (global or shared memory) with the whole
+// block (any size up to 1024 threads, a multiple of 32; every thread calls it).
+__device__ __forceinline__ void build_tile_list(const int* counts, const int* offsets, int E, const TileList& tl) {
+    __shared__ int warp_sum[32];
+    __shared__ int base_s;
+    if (threadIdx.x == 0) base_s = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, rpt = tl.rows_per_tile;
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        const int n = e < E ? (counts[e] + rpt - 1) / rpt : 0;
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int v = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+            int wi = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += u;
+            }
+            warp_sum[lane] = wi - v;
+        }
+        __syncthreads();
+        const int start = base_s + warp_sum[warp] + incl - n;
+        for (int i = 0; i < n; ++i) {
+            tl.tile_e[start + i] = e;
+            tl.tile_r0[start + i] = offsets[e] + i * rpt;
+            tl.tile_first[start + i] = start;
+            tl.tile_cnt[start + i] = n;
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) base_s = start + n;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) tl.tiles[0] = base_s;
+}
+
 // Route histogram / stable counting sort, optionally emitting expert groups (route_plan.cu).
 cudaError_t launch_route_plan(const int32_t* ids, int P, int E, int cap, int32_t* counts,
                               int32_t* offsets, int32_t* sorted_pair, int32_t* pair_to_sorted,
                               int32_t* group_count, int32_t* group_expert, int32_t* group_start,
                               int32_t* group_ncols, int32_t* err, cudaStream_t stream);
 // The same permutation (no groups) over several blocks for many pairs; blk is scratch of
-// route_plan_wide_ws_bytes(P, E) bytes (route_plan.cu). Three launches.
+// route_plan_wide_ws_bytes(P, E) bytes (route_plan.cu). Three launches; with tl.tiles set the
+// middle one also builds the grouped tier's m-tile list.
 size_t route_plan_wide_ws_bytes(int P, int E);
 cudaError_t launch_route_plan_wide(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
                                    int32_t* sorted_pair, int32_t* pair_to_sorted, int32_t* blk,
-                                   int32_t* err, cudaStream_t stream);
+                                   int32_t* err, cudaStream_t stream, const TileList& tl);
 size_t route_plan_smem_bytes(int E);
 
 }  // namespace moe

@@ -33,55 +33,12 @@ namespace moe {
 
 // ---- tile list -----------------------------------------------------------------------------------
 
-// One block: m-tile list from the per-expert counts (ascending expert, 128 sorted rows per tile).
-// tiles[0] = number of m-tiles; tile_e[i], tile_r0[i] = expert and first sorted row of tile i;
-// tile_first[i], tile_cnt[i] = first m-tile and number of m-tiles of that expert.
+// One block: the m-tile list from the per-expert counts (after the single-block route plan; the
+// multi-block plan builds it in its middle launch).
 __global__ void __launch_bounds__(1024) prefill_tiles_kernel(const int32_t* __restrict__ counts,
-                                                             const int32_t* __restrict__ offsets,
-                                                             int E, int32_t* __restrict__ tiles,
-                                                             int32_t* __restrict__ tile_e,
-                                                             int32_t* __restrict__ tile_r0,
-                                                             int32_t* __restrict__ tile_first,
-                                                             int32_t* __restrict__ tile_cnt) {
-    __shared__ int warp_sum[32];
-    __shared__ int base_s;
-    if (threadIdx.x == 0) base_s = 0;
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
-        const int e = e0 + threadIdx.x;
-        const int n = e < E ? (counts[e] + prefill::kBM - 1) / prefill::kBM : 0;
-        int incl = n;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) warp_sum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const int v = lane < (blockDim.x >> 5) ? warp_sum[lane] : 0;
-            int wi = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, wi, o);
-                if (lane >= o) wi += u;
-            }
-            warp_sum[lane] = wi - v;
-        }
-        __syncthreads();
-        const int start = base_s + warp_sum[warp] + incl - n;
-        for (int i = 0; i < n; ++i) {
-            tile_e[start + i] = e;
-            tile_r0[start + i] = offsets[e] + i * prefill::kBM;
-            tile_first[start + i] = start;
-            tile_cnt[start + i] = n;
-        }
-        __syncthreads();
-        if (threadIdx.x == blockDim.x - 1) base_s = start + n;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) tiles[0] = base_s;
+                                                             const int32_t* __restrict__ offsets, int E,
+                                                             TileList tl) {
+    build_tile_list(counts, offsets, E, tl);
 }
 
 // ---- x prep ---------------------------------------------------------------------------------------
@@ -274,20 +231,23 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     const int P = T * topk;
     auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
     cudaError_t st;
+    const TileList tl{I32(L.tiles), I32(L.tile_e), I32(L.tile_r0), I32(L.tile_first), I32(L.tile_cnt),
+                      prefill::kBM};
     stage_mark(stream, "route_plan");
-    // many pairs: the multi-block plan (one block serialises ~32 rounds of 1024 pairs)
-    if (P >= kWidePlanPairs)
+    // many pairs: the multi-block plan (one block serialises ~32 rounds of 1024 pairs), which also
+    // builds the m-tile list
+    if (P >= kWidePlanPairs) {
         st = launch_route_plan_wide(ids, P, E, I32(L.counts), I32(L.offsets), I32(L.sorted_pair),
-                                    I32(L.pair_to_sorted), I32(L.plan_blk), err, stream);
-    else
+                                    I32(L.pair_to_sorted), I32(L.plan_blk), err, stream, tl);
+        if (st != cudaSuccess) return st;
+    } else {
         st = launch_route_plan(ids, P, E, 1, I32(L.counts), I32(L.offsets), I32(L.sorted_pair),
                                I32(L.pair_to_sorted), nullptr, nullptr, nullptr, nullptr, err, stream);
-    if (st != cudaSuccess) return st;
-    stage_mark(stream, "tile_list");
-    prefill_tiles_kernel<<<1, 1024, 0, stream>>>(I32(L.counts), I32(L.offsets), E, I32(L.tiles),
-                                                 I32(L.tile_e), I32(L.tile_r0), I32(L.tile_first),
-                                                 I32(L.tile_cnt));
-    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+        if (st != cudaSuccess) return st;
+        stage_mark(stream, "tile_list");
+        prefill_tiles_kernel<<<1, 1024, 0, stream>>>(I32(L.counts), I32(L.offsets), E, tl);
+        if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    }
     uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
     // a finite clamp limit L <= 255 bounds |a| = |silu(min(g, L)) * clamp(u, -L, L)| by L^2, which
     // f16 holds without a range scale: the TMEM core then writes a in f16 itself

@@ -149,6 +149,9 @@ route_plan_kernel(const int32_t* __restrict__ ids, int P, int E, int cap,
 }
 
 // ---- the same permutation for many pairs, over several blocks --------------------------------------
+
+// shared memory up to which plan_base_kernel stages the per-block counts
+constexpr size_t kPlanStageBytes = 160 * 1024;
 // Block b owns pairs [b*kPlanThreads, (b+1)*kPlanThreads). plan_hist_kernel counts each block's
 // pairs per expert; plan_base_kernel turns the counts into each (block, expert) first position -
 // the expert's offset plus the counts of the earlier blocks - and the offsets; plan_scatter_kernel
@@ -176,19 +179,28 @@ plan_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restr
     for (int e = tid; e < E; e += kPlanThreads) blk[static_cast<size_t>(blockIdx.x) * E + e] = cnt[e];
 }
 
+// staged: the [nblk][E] counts go through shared memory (one coalesced read and write of blk
+// instead of nblk dependent accesses per expert in each of two passes)
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_base_kernel(int P, int E, int nblk, int32_t* __restrict__ blk, int32_t* __restrict__ counts,
-                 int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair) {
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair, int staged, TileList tl) {
     extern __shared__ __align__(16) int smem_i[];
     int* cnt = smem_i;                 // [E]
     int* run = cnt + E;                // [E]
+    int* bc = run + E;                 // [nblk][E] when staged
     __shared__ int scratch[33];
     const int tid = threadIdx.x;
+    const size_t nall = static_cast<size_t>(nblk) * E;
+    if (staged) {
+        for (size_t i = tid; i < nall; i += kPlanThreads) bc[i] = blk[i];
+        __syncthreads();
+    }
+    int* src = staged ? bc : blk;
     // per expert: block bases relative to the expert, and its total
     for (int e = tid; e < E; e += kPlanThreads) {
         int acc = 0;
         for (int b = 0; b < nblk; ++b) {
-            int32_t* q = blk + static_cast<size_t>(b) * E + e;
+            int* q = src + static_cast<size_t>(b) * E + e;
             const int c = *q;
             *q = acc;
             acc += c;
@@ -197,13 +209,19 @@ plan_base_kernel(int P, int E, int nblk, int32_t* __restrict__ blk, int32_t* __r
     }
     __syncthreads();
     const int total = block_exclusive_scan(cnt, run, E, scratch);
+    if (staged) {
+        for (size_t i = tid; i < nall; i += kPlanThreads) blk[i] = bc[i] + run[i % E];
+    } else {
+        for (int e = tid; e < E; e += kPlanThreads)
+            for (int b = 0; b < nblk; ++b) blk[static_cast<size_t>(b) * E + e] += run[e];
+    }
     for (int e = tid; e < E; e += kPlanThreads) {
         counts[e] = cnt[e];
         offsets[e] = run[e];
-        for (int b = 0; b < nblk; ++b) blk[static_cast<size_t>(b) * E + e] += run[e];
     }
     if (tid == 0) offsets[E] = total;
     for (int s = total + tid; s < P; s += kPlanThreads) sorted_pair[s] = -1;
+    if (tl.tiles != nullptr) build_tile_list(cnt, run, E, tl);   // cnt / run are final here
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
@@ -239,9 +257,12 @@ size_t route_plan_wide_ws_bytes(int P, int E) {
 
 cudaError_t launch_route_plan_wide(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets,
                                    int32_t* sorted_pair, int32_t* pair_to_sorted, int32_t* blk,
-                                   int32_t* err, cudaStream_t stream) {
+                                   int32_t* err, cudaStream_t stream, const TileList& tl) {
     const int nblk = (P + kPlanThreads - 1) / kPlanThreads;
-    const size_t s1 = static_cast<size_t>(E) * 4, s2 = static_cast<size_t>(E) * 8,
+    // the per-block counts fit shared memory beside the two [E] arrays: stage them
+    const size_t staged_bytes = (static_cast<size_t>(nblk) + 2) * E * 4;
+    const bool staged = staged_bytes <= kPlanStageBytes;
+    const size_t s1 = static_cast<size_t>(E) * 4, s2 = staged ? staged_bytes : static_cast<size_t>(E) * 8,
                  s3 = static_cast<size_t>(E) * 32;
     const void* fns[3] = {reinterpret_cast<const void*>(plan_hist_kernel),
                           reinterpret_cast<const void*>(plan_base_kernel),
@@ -254,7 +275,8 @@ cudaError_t launch_route_plan_wide(const int32_t* ids, int P, int E, int32_t* co
             if (st != cudaSuccess) return st;
         }
     plan_hist_kernel<<<nblk, kPlanThreads, s1, stream>>>(ids, P, E, blk, err);
-    plan_base_kernel<<<1, kPlanThreads, s2, stream>>>(P, E, nblk, blk, counts, offsets, sorted_pair);
+    plan_base_kernel<<<1, kPlanThreads, s2, stream>>>(P, E, nblk, blk, counts, offsets, sorted_pair,
+                                                      staged ? 1 : 0, tl);
     plan_scatter_kernel<<<nblk, kPlanThreads, s3, stream>>>(ids, P, E, blk, sorted_pair, pair_to_sorted);
     return cudaGetLastError();
 }

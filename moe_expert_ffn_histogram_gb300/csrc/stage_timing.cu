@@ -1,5 +1,9 @@
-// Stage timing: CUDA events recorded on the forward's own stream between its kernel launches.
+// Stage hooks. NVTX: every forward opens a range named after its entry point and, inside it, one
+// range per stage (route plan, gate/up, down and combine, ...), on the calling host thread, so
+// that a profiler can select a stage's kernels (ncu --nvtx --nvtx-include). Always on unless
+// built with MOE_NVTX=0; without an attached tool an NVTX call is a null-pointer check.
 //
+// Stage timing: CUDA events recorded on the forward's own stream between its kernel launches.
 // Off by default. When on, each forward records one event at the start of every stage and one
 // after the last; moe_stage_times turns the most recent forward's events into per-stage
 // durations. The events sit between launches, so a stage that normally starts early as a
@@ -9,9 +13,32 @@
 #include "stage_timing.cuh"
 #include "../../include/moe_ffn.h"
 
+#ifndef MOE_NVTX
+#define MOE_NVTX 1
+#endif
+#if MOE_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace moe {
 
 namespace {
+
+// NVTX: the calling host thread's open stage range (closed by the next stage or the call's end)
+thread_local bool t_stage_open = false;
+
+void nvtx_push(const char* name) {
+#if MOE_NVTX
+    nvtxRangePushA(name);
+#else
+    (void)name;
+#endif
+}
+void nvtx_pop() {
+#if MOE_NVTX
+    nvtxRangePop();
+#endif
+}
 
 constexpr int kMaxMarks = 64;
 
@@ -39,17 +66,25 @@ bool create_events() {
 
 }  // namespace
 
-void stage_begin(cudaStream_t) {
+void stage_begin(cudaStream_t, const char* call) {
+    nvtx_push(call);
+    t_stage_open = false;
     if (g_rec.on) g_rec.n = 0;
 }
 
 void stage_mark(cudaStream_t s, const char* name) {
+    if (t_stage_open) nvtx_pop();
+    nvtx_push(name);
+    t_stage_open = true;
     if (!g_rec.on || g_rec.n >= kMaxMarks - 1) return;
     if (cudaEventRecord(g_rec.ev[g_rec.n], s) != cudaSuccess) return;
     g_rec.name[g_rec.n++] = name;
 }
 
 void stage_end(cudaStream_t s) {
+    if (t_stage_open) nvtx_pop();
+    t_stage_open = false;
+    nvtx_pop();
     if (!g_rec.on || g_rec.n == 0) return;
     if (cudaEventRecord(g_rec.ev[g_rec.n], s) != cudaSuccess) return;
     g_rec.done = g_rec.n;

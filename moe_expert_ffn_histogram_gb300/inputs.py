@@ -157,7 +157,9 @@ class Fp8Bank:
 @dataclasses.dataclass
 class Nvfp4Bank:
     """Packed E2M1 codes (element 2j in the low nibble of byte j), one E4M3 scale byte per 16
-    elements along K, and one fp32 scale_2 per projection. gate/up [E, I, H/2], down [E, H, I/2]."""
+    elements along K, and one fp32 scale_2 per projection - or, in a bank from
+    make_nvfp4_bank_expert_scale2, one per expert and projection (float32 tensors [E]).
+    gate/up [E, I, H/2], down [E, H, I/2]."""
     w_gate: torch.Tensor
     sf_gate: torch.Tensor
     scale2_gate: float
@@ -173,8 +175,14 @@ class Nvfp4Bank:
         sel = (lambda t: t) if experts is None else (lambda t: t.index_select(0, experts.to(t.device)))
         d = {k: sel(getattr(self, k)).cpu().numpy()
              for k in ("w_gate", "sf_gate", "w_up", "sf_up", "w_down", "sf_down")}
-        d.update(scale2_gate=self.scale2_gate, scale2_up=self.scale2_up, scale2_down=self.scale2_down)
+        for k in ("scale2_gate", "scale2_up", "scale2_down"):
+            v = getattr(self, k)
+            d[k] = sel(v).cpu().numpy().astype(np.float32) if isinstance(v, torch.Tensor) else v
         return d
+
+    @property
+    def per_expert_scale2(self) -> bool:
+        return isinstance(self.scale2_gate, torch.Tensor)
 
 
 def quantize_e4m3_blocks(w: torch.Tensor):
@@ -274,6 +282,26 @@ def make_nvfp4_bank(E: int, H: int, I: int, seed: int, device="cpu", experts=Non
     return Nvfp4Bank(out["gate"][0], out["gate"][1], scale2["gate"],
                      out["up"][0], out["up"][1], scale2["up"],
                      out["down"][0], out["down"][1], scale2["down"])
+
+
+def make_nvfp4_bank_expert_scale2(E: int, H: int, I: int, seed: int, device="cpu") -> Nvfp4Bank:
+    """The same matrices as make_nvfp4_bank, each expert quantised with its own scale_2 per
+    projection (its amax / (6 * 448), as a per-expert checkpoint stores it), held as float32
+    tensors [E] on the bank's device."""
+    shapes = {"gate": (I, H), "up": (I, H), "down": (H, I)}
+    out = {}
+    for proj, (n, k) in shapes.items():
+        packed = torch.empty(E, n, k // 2, dtype=torch.uint8, device=device)
+        sf = torch.empty(E, n, k // 16, dtype=torch.uint8, device=device)
+        s2 = torch.empty(E, dtype=torch.float32)
+        for e in range(E):
+            m = _normal_matrix(seed, e, proj, n, k, device)
+            s2[e] = float(np.float32(float(m.abs().amax()) / (E2M1_MAX * E4M3_MAX)))
+            p, s = quantize_nvfp4(m, float(s2[e]))
+            packed[e].copy_(p)
+            sf[e].copy_(s)
+        out[proj] = (packed, sf, s2.to(device))
+    return Nvfp4Bank(*out["gate"], *out["up"], *out["down"])
 
 
 # ---- whole workloads ---------------------------------------------------------------------------

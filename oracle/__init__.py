@@ -59,6 +59,7 @@ def _load():
         lib.oracle_hardware_threads.restype = ctypes.c_int
         for name in ("oracle_combine", "oracle_dequant_fp8", "oracle_dequant_nvfp4",
                      "oracle_route_permute", "oracle_moe_fp8", "oracle_moe_nvfp4",
+                     "oracle_moe_nvfp4_expert_scale2",
                      "oracle_router_logits", "oracle_router_topk", "oracle_shared_expert",
                      "oracle_layer_epilogue"):
             getattr(lib, name).restype = ctypes.c_int
@@ -179,7 +180,8 @@ def _forward(kind, x_bf16_bits, ids, wts, bank, limit, tokens=None, intermediate
         inter["y"] = np.zeros((nt * topk, H), np.float64)
     ip = lambda k: _ptr(inter[k]) if intermediates else None  # noqa: E731
     arrs = {k: _c(v, np.float32 if k.startswith("s_") else np.uint8)
-            for k, v in bank.items() if isinstance(v, np.ndarray)}
+            for k, v in bank.items() if isinstance(v, np.ndarray) and not k.startswith("scale2")}
+    per_expert = kind == "nvfp4" and isinstance(bank["scale2_gate"], np.ndarray)
     if kind == "fp8":
         rc = lib.oracle_moe_fp8(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
                                 _ptr(arrs["w_gate"]), _ptr(arrs["s_gate"]),
@@ -187,6 +189,16 @@ def _forward(kind, x_bf16_bits, ids, wts, bank, limit, tokens=None, intermediate
                                 _ptr(arrs["w_down"]), _ptr(arrs["s_down"]),
                                 ctypes.c_double(limit), _ptr(tok), nt, _ptr(out), _ptr(outb),
                                 ip("g"), ip("u"), ip("a"), ip("y"), int(nthreads), _ptr(err))
+    elif per_expert:                   # one scale_2 per expert and projection, [E] float32 each
+        s2 = {k: _c(bank[k], np.float32) for k in ("scale2_gate", "scale2_up", "scale2_down")}
+        if any(v.shape != (E,) for v in s2.values()):
+            raise ValueError("per-expert scale_2 arrays must have shape [E]")
+        rc = lib.oracle_moe_nvfp4_expert_scale2(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
+                                                _ptr(arrs["w_gate"]), _ptr(arrs["sf_gate"]), _ptr(s2["scale2_gate"]),
+                                                _ptr(arrs["w_up"]), _ptr(arrs["sf_up"]), _ptr(s2["scale2_up"]),
+                                                _ptr(arrs["w_down"]), _ptr(arrs["sf_down"]), _ptr(s2["scale2_down"]),
+                                                1, ctypes.c_double(limit), _ptr(tok), nt, _ptr(out), _ptr(outb),
+                                                ip("g"), ip("u"), ip("a"), ip("y"), int(nthreads), _ptr(err))
     else:
         rc = lib.oracle_moe_nvfp4(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
                                   _ptr(arrs["w_gate"]), _ptr(arrs["sf_gate"]),
@@ -214,7 +226,8 @@ def moe_fp8(x_bf16_bits, ids, wts, bank, limit, tokens=None, intermediates=False
 
 
 def moe_nvfp4(x_bf16_bits, ids, wts, bank, limit, tokens=None, intermediates=False, nthreads=0):
-    """NVFP4 routed FFN. bank: w_* packed [E,N,K/2] u8, sf_* [E,N,K/16] u8, scale2_* floats."""
+    """NVFP4 routed FFN. bank: w_* packed [E,N,K/2] u8, sf_* [E,N,K/16] u8, scale2_* floats, or
+    float32 arrays [E] for one scale_2 per expert and projection."""
     return _forward("nvfp4", x_bf16_bits, ids, wts, bank, limit, tokens, intermediates, nthreads)
 
 

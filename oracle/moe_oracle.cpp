@@ -20,7 +20,10 @@
 //     scale_rows*scale_cols scales).
 //   * NVFP4 weight = e2m1(nibble) * e4m3(sf[n][k/16]) * scale_2, two codes per byte and one
 //     scale byte per 16 elements — dsv4_ep.rs, `chain` (wstride = inter*hidden/2,
-//     sstride = inter*hidden/16); scale_2 is a by-value f32 — forward.rs, `w4a16_gemv`.
+//     sstride = inter*hidden/16); scale_2 is a by-value f32 — forward.rs, `w4a16_gemv`. Or one
+//     scale_2 per expert and projection (oracle_moe_nvfp4_expert_scale2) — forward.rs,
+//     `w4a16_gemv_moe` (the expert table's scale2_vals) and dsv4_ep.rs's EP matrix test (one
+//     macro scale per expert and projection).
 //   * Route permutation: per-expert counts, exclusive offsets, expert-sorted pair list and its
 //     inverse — forward.rs, `Glm5NextMlpWorkspace` (sorted ids, expert_offsets[E+1],
 //     token_to_perm). Ties inside one expert are broken by ascending pair index t*top_k+k
@@ -131,6 +134,9 @@ struct Bank {
     const uint8_t* sf;          // NVFP4, [E][N][K/16] E4M3 bytes
     double scale_2;             // NVFP4
     int N, K;
+    // NVFP4 with one scale_2 per expert: expert e's is s2e[e * s2_stride] (null: scale_2 for all)
+    const float* s2e = nullptr;
+    int s2_stride = 1;
     // Dequantised W[e][n][k].
     double w(int e, int n, int k) const {
         if (fmt == 1) {
@@ -142,7 +148,8 @@ struct Bank {
         const size_t byte = (static_cast<size_t>(e) * N + n) * (K / 2) + k / 2;
         const uint8_t nib = (k % 2 == 0) ? (codes[byte] & 0xF) : (codes[byte] >> 4);
         const size_t sfi = (static_cast<size_t>(e) * N + n) * (K / 16) + k / 16;
-        return e2m1_value(nib) * e4m3_value(sf[sfi]) * scale_2;
+        const double s2 = s2e != nullptr ? static_cast<double>(s2e[static_cast<size_t>(e) * s2_stride]) : scale_2;
+        return e2m1_value(nib) * e4m3_value(sf[sfi]) * s2;
     }
 };
 
@@ -373,6 +380,28 @@ int oracle_moe_nvfp4(const uint16_t* x, int T, int H, int I, int E, int topk, co
     Bank g{2, w_gate, nullptr, sf_gate, scale2_gate, I, H};
     Bank u{2, w_up, nullptr, sf_up, scale2_up, I, H};
     Bank d{2, w_down, nullptr, sf_down, scale2_down, H, I};
+    return moe_forward(x, T, H, I, E, topk, ids, wts, g, u, d, limit, token_list, n_tokens,
+                       out_f64, out_bf16, g_out, u_out, a_out, y_out, nthreads, err);
+}
+
+// The same with one scale_2 per expert and projection: expert e's is scale2_x[e * stride]
+// ("memra-engine 0.131.0 src/dsv4_ep.rs", the EP matrix test's macro scales, one per expert and
+// projection; "spark_model layers/glm5next_mlp/forward.rs", `w4a16_gemv_moe`: the expert table's
+// scale2_vals, one per expert).
+int oracle_moe_nvfp4_expert_scale2(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                   const int32_t* ids, const float* wts, const uint8_t* w_gate,
+                                   const uint8_t* sf_gate, const float* scale2_gate, const uint8_t* w_up,
+                                   const uint8_t* sf_up, const float* scale2_up, const uint8_t* w_down,
+                                   const uint8_t* sf_down, const float* scale2_down, int stride,
+                                   double limit, const int32_t* token_list, int n_tokens, double* out_f64,
+                                   uint16_t* out_bf16, double* g_out, double* u_out, double* a_out,
+                                   double* y_out, int nthreads, int32_t* err) {
+    if (!shapes_ok(T, H, I, E, topk)) return -2;
+    if (!(limit > 0.0)) return -4;
+    if (scale2_gate == nullptr || scale2_up == nullptr || scale2_down == nullptr || stride < 1) return -3;
+    Bank g{2, w_gate, nullptr, sf_gate, 0.0, I, H, scale2_gate, stride};
+    Bank u{2, w_up, nullptr, sf_up, 0.0, I, H, scale2_up, stride};
+    Bank d{2, w_down, nullptr, sf_down, 0.0, H, I, scale2_down, stride};
     return moe_forward(x, T, H, I, E, topk, ids, wts, g, u, d, limit, token_list, n_tokens,
                        out_f64, out_bf16, g_out, u_out, a_out, y_out, nthreads, err);
 }

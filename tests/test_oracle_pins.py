@@ -274,6 +274,68 @@ def test_nvfp4_ffn_matches_dense_bruteforce(T, H, I, E):
     assert np.allclose(r["out"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
 
 
+def _nvfp4_expert_scale2_case(T=3, H=256, I=128, E=6, seed=31):
+    bank = inputs.make_nvfp4_bank_expert_scale2(E, H, I, seed)
+    x = inputs.normal_activations(T, H, seed, "cpu", scale=2.0)
+    ids = inputs.make_routes("uniform", T, E, seed, min(8, E))
+    wts = inputs.softmax_route_weights(T, seed, min(8, E))
+    bits = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+    return bank, x, ids.numpy(), wts.numpy(), bits
+
+
+def test_nvfp4_expert_scale2_matches_dense_bruteforce():
+    """One scale_2 per expert and projection (a per-expert checkpoint): the oracle against dense
+    float64 matrices that multiply each expert's codes by its own scale_2."""
+    bank, x, ids, wts, bits = _nvfp4_expert_scale2_case()
+    b = bank.numpy()
+    assert len(set(b["scale2_gate"].tolist())) > 1          # the experts' values differ
+    r = oracle.moe_nvfp4(bits, ids, wts, b, inputs.LIMIT)
+    per = lambda k: b[k].astype(np.float64)[:, None, None]  # noqa: E731
+    ref = _bruteforce(x.to(torch.float64).numpy(), ids, wts,
+                      _dense_nvfp4(b["w_gate"], b["sf_gate"], per("scale2_gate")),
+                      _dense_nvfp4(b["w_up"], b["sf_up"], per("scale2_up")),
+                      _dense_nvfp4(b["w_down"], b["sf_down"], per("scale2_down")), inputs.LIMIT)
+    assert np.allclose(r["out"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_nvfp4_expert_scale2_equal_values_are_the_scalar_path():
+    bank, x, ids, wts, bits = _nvfp4_expert_scale2_case()
+    b = bank.numpy()
+    scalar = dict(b)
+    for k in ("scale2_gate", "scale2_up", "scale2_down"):
+        scalar[k] = float(b[k][2])
+        b[k] = np.full_like(b[k], b[k][2])
+    r1 = oracle.moe_nvfp4(bits, ids, wts, b, inputs.LIMIT)
+    r2 = oracle.moe_nvfp4(bits, ids, wts, scalar, inputs.LIMIT)
+    assert np.array_equal(r1["out"], r2["out"])
+
+
+def test_nvfp4_expert_scale2_power_of_two_equals_scale_byte_shift():
+    """scale_2 * 2^j for expert e is the same weight as adding j to the exponent field of each of
+    e's E4M3 scale bytes (exact in float64): per-expert powers of two against the scalar path on
+    the shifted bytes, bit for bit - an index or projection mix-up in the per-expert lookup
+    cannot pass."""
+    T, H, I, E = 3, 256, 128, 6
+    rng = np.random.default_rng(7)
+    base = inputs.make_custom("nvfp4", T, H, I, E, seed=41, topk=min(8, E), x_scale=2.0)
+    b = base.bank.numpy()
+    for k in ("sf_gate", "sf_up", "sf_down"):                 # exponents 3..11, any sign/mantissa
+        exp_ = rng.integers(3, 12, b[k].shape)
+        b[k] = ((rng.integers(0, 2, b[k].shape) << 7) | (exp_ << 3) | rng.integers(0, 8, b[k].shape)).astype(np.uint8)
+    shifted = dict(b)
+    per = dict(b)
+    for k, sk in (("scale2_gate", "sf_gate"), ("scale2_up", "sf_up"), ("scale2_down", "sf_down")):
+        j = rng.integers(-2, 3, E)
+        per[k] = (np.float32(b[k]) * np.exp2(j)).astype(np.float32)
+        e_field = ((b[sk] >> 3) & 0xF).astype(np.int64) + j[:, None, None]
+        assert e_field.min() >= 1 and e_field.max() <= 13
+        shifted[sk] = ((b[sk] & 0x87) | (e_field << 3)).astype(np.uint8)
+    ids, wts = base.ids.numpy(), base.wts.numpy()
+    r1 = oracle.moe_nvfp4(base.x_bits(), ids, wts, per, base.limit)
+    r2 = oracle.moe_nvfp4(base.x_bits(), ids, wts, shifted, base.limit)
+    assert np.array_equal(r1["out"], r2["out"])
+
+
 def test_oracle_intermediates_and_token_subset():
     wl = inputs.make_custom("fp8", 4, 256, 128, 12, seed=3)
     b = wl.bank.numpy()

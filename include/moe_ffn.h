@@ -170,6 +170,33 @@ MOE_API int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int
                       int32_t* err, void* stream);
 
 /*
+ * moe_nvfp4_forward_expert_scale2 - moe_nvfp4_forward with one scale_2 per expert and projection,
+ * as a checkpoint quantised expert by expert stores it:
+ *   W[e][n][k] = e2m1(nibble) * e4m3(sf[e][n][k/16]) * scale2_x[e * scale2_stride]
+ * ("spark_model layers/glm5next_mlp/forward.rs", `w4a16_gemv_moe`: the expert table passes its
+ * scale2_vals, one per expert; "memra-engine 0.131.0 src/dsv4_ep.rs", the EP matrix test: one
+ * macro scale per expert and projection).
+ *   scale2_gate, scale2_up, scale2_down  device fp32 arrays, 4-byte aligned; expert e's value at
+ *                 element e * scale2_stride, so separate [E] arrays (stride 1) and one [E][3]
+ *                 table (the three pointers offset by the projection's column, stride 3) both work.
+ *   scale2_stride >= 1.
+ * Everything else (sizes, tiers, workspace, err, stream, arithmetic) as moe_nvfp4_forward, the
+ * per-expert value taking the scalar's place in each tier. The values are read on the device:
+ * they are not checked, and a non-finite one makes that expert's outputs non-finite.
+ * Errors: MOE_ERR_NULL for a null table, MOE_ERR_VALUE for scale2_stride < 1 (and as
+ * moe_nvfp4_forward), MOE_ERR_ALIGN for a table that is not 4-byte aligned.
+ */
+MOE_API int moe_nvfp4_forward_expert_scale2(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                            const int32_t* topk_ids, const float* topk_weights,
+                                            const uint8_t* w_gate, const uint8_t* sf_gate,
+                                            const float* scale2_gate, const uint8_t* w_up,
+                                            const uint8_t* sf_up, const float* scale2_up,
+                                            const uint8_t* w_down, const uint8_t* sf_down,
+                                            const float* scale2_down, int scale2_stride, float limit,
+                                            uint16_t* out, void* workspace, size_t workspace_bytes,
+                                            int32_t* err, void* stream);
+
+/*
  * moe_fp8_forward_layer / moe_nvfp4_forward_layer - the forwards above with the MoE layer's
  * epilogue fused into the combine: out = bf16(((sum_k w[t,k] * y[t,k]) + shared[t]) + residual[t]),
  * the two adds in fp32 in that order after the slot-order sum, one rounding

@@ -29,7 +29,8 @@ EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_
             "moe_nvfp4_down_combine", "moe_build_arch", "moe_fp8_forward_noalloc",
             "moe_router_workspace_bytes", "moe_router", "moe_fp8_forward_layer",
             "moe_nvfp4_forward_layer", "moe_shared_expert_workspace_bytes", "moe_shared_expert_bf16",
-            "moe_stage_timing", "moe_stage_times", "moe_test_barrier_timeout")
+            "moe_stage_timing", "moe_stage_times", "moe_test_barrier_timeout",
+            "moe_nvfp4_forward_expert_scale2")
 
 _lib = None
 
@@ -65,6 +66,9 @@ def load(path: Optional[str] = None):
     lib.moe_nvfp4_forward.restype = i32
     lib.moe_nvfp4_forward.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, vp,
                                       f32, vp, vp, f32, f32, vp, vp, sz, vp, vp]
+    lib.moe_nvfp4_forward_expert_scale2.restype = i32
+    lib.moe_nvfp4_forward_expert_scale2.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                    vp, vp, vp, vp, vp, i32, f32, vp, vp, sz, vp, vp]
     lib.moe_plan.restype = i32
     lib.moe_plan.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, vp]
     lib.moe_fp8_gate_up.restype = i32
@@ -205,11 +209,26 @@ def fp8_forward(x, ids, wts, bank, limit: float, out=None, workspace=None, err=N
 
 
 def nvfp4_forward(x, ids, wts, bank, limit: float, out=None, workspace=None, err=None, stream=None):
-    """Routed MoE FFN over an NVFP4 (W4A16) bank (moe_nvfp4_forward)."""
+    """Routed MoE FFN over an NVFP4 (W4A16) bank (moe_nvfp4_forward; with one scale_2 per expert
+    and projection, moe_nvfp4_forward_expert_scale2)."""
     E, I, _ = bank.w_gate.shape
     dev, T, H, topk, out, ws = _common(x, ids, wts, out, workspace, err, FMT_NVFP4, E, I)
     for n in ("w_gate", "w_up", "w_down", "sf_gate", "sf_up", "sf_down"):
         _need(getattr(bank, n), n, torch.uint8, dev)
+    if _per_expert_scale2(bank):
+        for n in ("scale2_gate", "scale2_up", "scale2_down"):
+            t = getattr(bank, n)
+            _need(t, n, torch.float32, dev)
+            if tuple(t.shape) != (E,):
+                raise ValueError(f"{n} must be [E] per expert")
+        rc = load().moe_nvfp4_forward_expert_scale2(
+            _ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
+            _ptr(bank.w_gate), _ptr(bank.sf_gate), _ptr(bank.scale2_gate),
+            _ptr(bank.w_up), _ptr(bank.sf_up), _ptr(bank.scale2_up),
+            _ptr(bank.w_down), _ptr(bank.sf_down), _ptr(bank.scale2_down), 1,
+            float(limit), _ptr(out), _ptr(ws), ws.numel(), _ptr(err), _stream(dev, stream))
+        _check("moe_nvfp4_forward_expert_scale2", rc)
+        return out
     rc = load().moe_nvfp4_forward(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
                                   _ptr(bank.w_gate), _ptr(bank.sf_gate), float(bank.scale2_gate),
                                   _ptr(bank.w_up), _ptr(bank.sf_up), float(bank.scale2_up),
@@ -218,6 +237,16 @@ def nvfp4_forward(x, ids, wts, bank, limit: float, out=None, workspace=None, err
                                   _stream(dev, stream))
     _check("moe_nvfp4_forward", rc)
     return out
+
+
+def _per_expert_scale2(bank) -> bool:
+    return isinstance(getattr(bank, "scale2_gate", None), torch.Tensor)
+
+
+def _scalar_scale2_only(bank, fn: str):
+    if _per_expert_scale2(bank):
+        raise ValueError(f"{fn} takes one scale_2 per projection; a bank with one per expert goes "
+                         "through nvfp4_forward (moe_nvfp4_forward_expert_scale2)")
 
 
 def forward(x, ids, wts, bank, limit: float, **kw):
@@ -230,6 +259,7 @@ def forward(x, ids, wts, bank, limit: float, **kw):
 def forward_layer(x, ids, wts, bank, limit: float, shared=None, residual=None, out=None,
                   workspace=None, err=None, stream=None):
     """moe_*_forward_layer: the forward with out = bf16((routed + shared) + residual)."""
+    _scalar_scale2_only(bank, "forward_layer")
     E, I, _ = bank.w_gate.shape
     fmt = FMT_FP8 if bank.fmt == "fp8" else FMT_NVFP4
     dev, T, H, topk, out, ws = _common(x, ids, wts, out, workspace, err, fmt, E, I)
@@ -289,6 +319,7 @@ def plan(ids, H, I, E, fmt, workspace, err=None, stream=None):
 
 
 def gate_up(x, ids, bank, limit, workspace, err=None, stream=None):
+    _scalar_scale2_only(bank, "gate_up")
     T, H = x.shape
     topk = ids.shape[1]
     E, I, _ = bank.w_gate.shape
@@ -308,6 +339,7 @@ def gate_up(x, ids, bank, limit, workspace, err=None, stream=None):
 
 
 def down_combine(ids, wts, bank, out, workspace, stream=None):
+    _scalar_scale2_only(bank, "down_combine")
     T, H = out.shape
     topk = ids.shape[1]
     E, I, _ = bank.w_gate.shape

@@ -143,12 +143,21 @@ int stage_plan(int rows, int E, int topk, const int32_t* ids, const Ws& w, int32
         w.at<int32_t>(w.L.group_ncols), err, s));
 }
 
+// NVFP4 with one scale_2 per expert and projection: expert e's gate value is g[e * stride]
+// (all null: the projections' scalars)
+struct ExpertScale2 {
+    const float* g = nullptr;
+    const float* u = nullptr;
+    const float* d = nullptr;
+    int stride = 1;
+};
+
 template <int FMT>
 int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, const int32_t* ids,
                   const uint8_t* wg, const float* sg, const uint8_t* sfg, float s2g,
                   const uint8_t* wu, const float* su, const uint8_t* sfu, float s2u, float limit,
                   const Ws& w, int32_t* err, cudaStream_t s, const uint8_t* wd = nullptr,
-                  const uint8_t* sfd = nullptr) {
+                  const uint8_t* sfd = nullptr, const ExpertScale2& xs2 = {}) {
     GateUpArgs a{};
     a.x = reinterpret_cast<const __nv_bfloat16*>(x);
     a.H = H;
@@ -161,6 +170,9 @@ int stage_gate_up(const uint16_t* x, int rows, int H, int I, int E, int topk, co
     a.sfu = sfu;
     a.s2g = s2g;
     a.s2u = s2u;
+    a.s2g_e = xs2.g;
+    a.s2u_e = xs2.u;
+    a.s2_stride = xs2.stride;
     a.limit = limit;
     a.grp = groups_for(w, ids, rows, topk, E);
     a.act = w.at<__half>(w.L.act);
@@ -187,7 +199,7 @@ template <int FMT>
 int stage_down(int rows, int H, int I, int E, int topk, const int32_t* ids, const float* wts,
                const uint8_t* wd, const float* sd, const uint8_t* sfd, float s2d, uint16_t* out,
                const Ws& w, cudaStream_t s, const uint16_t* shared = nullptr,
-               const uint16_t* residual = nullptr) {
+               const uint16_t* residual = nullptr, const ExpertScale2& xs2 = {}) {
     DownArgs a{};
     a.T = rows;
     a.H = H;
@@ -200,6 +212,8 @@ int stage_down(int rows, int H, int I, int E, int topk, const int32_t* ids, cons
     a.sd = sd;
     a.sfd = sfd;
     a.s2d = s2d;
+    a.s2d_e = xs2.d;
+    a.s2_stride = xs2.stride;
     a.grp = groups_for(w, ids, rows, topk, E);
     a.act = w.at<__half>(w.L.act);
     a.act_scale = w.at<float>(w.L.act_scale);
@@ -218,7 +232,8 @@ int stage_fused(const uint16_t* x, int rows, int H, int I, int E, int topk, cons
                 const uint8_t* wu, const float* su, const uint8_t* sfu, float s2u,
                 const uint8_t* wd, const float* sd, const uint8_t* sfd, float s2d, float limit,
                 uint16_t* out, const Ws& w, int32_t* err, cudaStream_t s,
-                const uint16_t* shared = nullptr, const uint16_t* residual = nullptr) {
+                const uint16_t* shared = nullptr, const uint16_t* residual = nullptr,
+                const ExpertScale2& xs2 = {}) {
     Groups grp{};
     grp.ids = ids;
     grp.topk = topk;
@@ -235,6 +250,9 @@ int stage_fused(const uint16_t* x, int rows, int H, int I, int E, int topk, cons
     ga.sfu = sfu;
     ga.s2g = s2g;
     ga.s2u = s2u;
+    ga.s2g_e = xs2.g;
+    ga.s2u_e = xs2.u;
+    ga.s2_stride = xs2.stride;
     ga.limit = limit;
     ga.grp = grp;
     ga.act = w.at<__half>(w.L.act);
@@ -252,6 +270,8 @@ int stage_fused(const uint16_t* x, int rows, int H, int I, int E, int topk, cons
     da.sd = sd;
     da.sfd = sfd;
     da.s2d = s2d;
+    da.s2d_e = xs2.d;
+    da.s2_stride = xs2.stride;
     da.grp = grp;
     da.act = ga.act;
     da.act_scale = ga.act_scale;
@@ -273,7 +293,7 @@ template <int FMT>
 int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32_t* ids,
             const float* wts, Proj pg, Proj pu, Proj pd, float limit, uint16_t* out, void* ws,
             size_t ws_bytes, int32_t* err, cudaStream_t s, const uint16_t* shared = nullptr,
-            const uint16_t* residual = nullptr) {
+            const uint16_t* residual = nullptr, const ExpertScale2& xs2 = {}) {
     int rc = check_sizes(T, H, I, E, topk);
     if (rc) return rc;
     StageScope timing(s, FMT == 0 ? "moe_fp8_forward" : "moe_nvfp4_forward");
@@ -281,7 +301,8 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
         if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
         const PrefillLayout L = prefill_layout(T, H, I, E, topk);
         if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-        PrefillWeights wt{pg.w, pu.w, pd.w, pg.s, pu.s, pd.s, pg.sf, pu.sf, pd.sf, pg.s2, pu.s2, pd.s2};
+        PrefillWeights wt{pg.w,  pu.w,  pd.w,  pg.s, pu.s, pd.s, pg.sf, pu.sf, pd.sf, pg.s2, pu.s2, pd.s2,
+                          xs2.g, xs2.u, xs2.d, xs2.stride};
         return cuda_status(launch_prefill(FMT, reinterpret_cast<const __nv_bfloat16*>(x), T, H, I, E, topk,
                                           ids, wts, wt, limit, reinterpret_cast<__nv_bfloat16*>(out),
                                           static_cast<uint8_t*>(ws), L, err, s,
@@ -307,18 +328,18 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
             stage_mark(s, "fused");
             if ((rc = stage_fused<FMT>(x_g, rows, H, I, E, topk, ids_g, wts_g, pg.w, pg.s, pg.sf,
                                        pg.s2, pu.w, pu.s, pu.sf, pu.s2, pd.w, pd.s, pd.sf, pd.s2,
-                                       limit, out_g, w, err, s, sh_g, rs_g)))
+                                       limit, out_g, w, err, s, sh_g, rs_g, xs2)))
                 return rc;
         } else {
             stage_mark(s, "plan");
             if ((rc = stage_plan(rows, E, topk, ids_g, w, err, s))) return rc;
             stage_mark(s, "gate_up");
             if ((rc = stage_gate_up<FMT>(x_g, rows, H, I, E, topk, ids_g, pg.w, pg.s, pg.sf, pg.s2,
-                                         pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s, pd.w, pd.sf)))
+                                         pu.w, pu.s, pu.sf, pu.s2, limit, w, err, s, pd.w, pd.sf, xs2)))
                 return rc;
             stage_mark(s, "down_combine");
             if ((rc = stage_down<FMT>(rows, H, I, E, topk, ids_g, wts_g, pd.w, pd.s, pd.sf, pd.s2,
-                                      out_g, w, s, sh_g, rs_g)))
+                                      out_g, w, s, sh_g, rs_g, xs2)))
                 return rc;
         }
         start += rows;
@@ -391,6 +412,27 @@ int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
                       Proj{w_up, nullptr, sf_up, scale2_up},
                       Proj{w_down, nullptr, sf_down, scale2_down}, limit, out, workspace,
                       workspace_bytes, err, static_cast<cudaStream_t>(stream));
+}
+
+int moe_nvfp4_forward_expert_scale2(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                    const int32_t* topk_ids, const float* topk_weights,
+                                    const uint8_t* w_gate, const uint8_t* sf_gate, const float* scale2_gate,
+                                    const uint8_t* w_up, const uint8_t* sf_up, const float* scale2_up,
+                                    const uint8_t* w_down, const uint8_t* sf_down, const float* scale2_down,
+                                    int scale2_stride, float limit, uint16_t* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!x || !topk_ids || !topk_weights || !w_gate || !sf_gate || !w_up || !sf_up || !w_down ||
+        !sf_down || !out || !scale2_gate || !scale2_up || !scale2_down)
+        return MOE_ERR_NULL;
+    if (!limit_ok(limit) || scale2_stride < 1) return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, w_down, sf_gate, sf_up, sf_down, out)) return MOE_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(scale2_gate) | reinterpret_cast<uintptr_t>(scale2_up) |
+         reinterpret_cast<uintptr_t>(scale2_down)) & 3u)
+        return MOE_ERR_ALIGN;
+    return forward<1>(x, T, H, I, E, topk, topk_ids, topk_weights, Proj{w_gate, nullptr, sf_gate, 1.f},
+                      Proj{w_up, nullptr, sf_up, 1.f}, Proj{w_down, nullptr, sf_down, 1.f}, limit, out,
+                      workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream), nullptr, nullptr,
+                      ExpertScale2{scale2_gate, scale2_up, scale2_down, scale2_stride});
 }
 
 // ---- the forwards with the layer epilogue ---------------------------------------------------

@@ -219,7 +219,8 @@ __global__ void __launch_bounds__(kItemThreads, 2) fp4_token_gate_up_kernel(cons
     // ---- epilogue: scales, clamped SwiGLU, per-64-block range scale, f16 store ----
     float hv = 0.0f;
     if (c == 0) {
-        const float gv = accg * sh.x_inv[0] * a.s2g, uv = accu * sh.x_inv[0] * a.s2u;
+        const float gv = accg * sh.x_inv[0] * scale2_of(a.s2g, a.s2g_e, a.s2_stride, e),
+                    uv = accu * sh.x_inv[0] * scale2_of(a.s2u, a.s2u_e, a.s2_stride, e);
         hv = clamped_swiglu(gv, uv, a.limit);
     }
     const float m = warp_max(fabsf(hv));
@@ -346,8 +347,10 @@ __global__ void __launch_bounds__(kItemThreads, 3) fp4_token_down_kernel(const D
     accB += __shfl_xor_sync(0xffffffffu, accB, 1);
     accB += __shfl_xor_sync(0xffffffffu, accB, 2);
     if (c == 0 && k < a.topk) {
-        ys[k][g] = accA * a.s2d;
-        ys[k][g + 8] = accB * a.s2d;
+        const int ek = a.ids[k];                            // reloaded: not kept live through the loop
+        const float s2 = ek >= 0 && ek < a.E ? scale2_of(a.s2d, a.s2d_e, a.s2_stride, ek) : 0.0f;
+        ys[k][g] = accA * s2;
+        ys[k][g + 8] = accB * s2;
     }
     __syncthreads();
     // slot-order combine: one thread per output row; a separate rounded multiply and add per term

@@ -387,8 +387,8 @@ __device__ void gate_up_item(const GateUpArgs& a, const GroupView& gv, int fb, _
         if (col < ncols) {
             float gv_ = acc[j] * sh.x_inv[col], uv = acc[2 + j] * sh.x_inv[col];
             if constexpr (FMT == 1) {
-                gv_ *= a.s2g;
-                uv *= a.s2u;
+                gv_ *= scale2_of(a.s2g, a.s2g_e, a.s2_stride, e);
+                uv *= scale2_of(a.s2u, a.s2u_e, a.s2_stride, e);
             }
             hv[j] = clamped_swiglu(gv_, uv, a.limit);
         }
@@ -567,7 +567,7 @@ __device__ void down_item(const DownArgs& a, const GroupList& gl, int jt, float*
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] *= a.s2d;
+            for (int i = 0; i < 4; ++i) acc[i] *= scale2_of(a.s2d, a.s2d_e, a.s2_stride, e);
         }
         if (p0 >= 0) {
             ys[p0 * kDownRows + g] = acc[0];

@@ -15,6 +15,10 @@ struct GateUpArgs {
     const uint8_t* sfg;   // NVFP4 scale bytes [E][I][H/16]
     const uint8_t* sfu;
     float s2g, s2u;       // NVFP4 scale_2
+    // NVFP4 with one scale_2 per expert: expert e's is s2g_e[e * s2_stride] (null: s2g for all)
+    const float* s2g_e;
+    const float* s2u_e;
+    int s2_stride;
     float limit;
     Groups grp;
     __half* act;          // [P][I] f16, range-scaled
@@ -27,6 +31,12 @@ struct GateUpArgs {
     const uint8_t* pf_wd;  // down codes [E][H][I/2]
     const uint8_t* pf_sfd; // down scale bytes [E][H][I/16]
 };
+
+// NVFP4 scale_2 of expert e: its entry of the per-expert table when there is one, else the
+// projection's scalar.
+__device__ __forceinline__ float scale2_of(float s2, const float* s2e, int stride, int e) {
+    return s2e != nullptr ? __ldg(s2e + static_cast<size_t>(e) * stride) : s2;
+}
 
 // Single-token NVFP4 calls ask L2 for their whole weight set up front (0: they do not).
 #ifndef MOE_FP4_L2_PREFETCH
@@ -42,6 +52,8 @@ struct DownArgs {
     const float* sd;        // FP8 block scales [E][H/128][I/128]
     const uint8_t* sfd;     // NVFP4 scale bytes [E][H][I/16]
     float s2d;
+    const float* s2d_e;     // NVFP4, one scale_2 per expert: s2d_e[e * s2_stride] (null: s2d)
+    int s2_stride;
     Groups grp;
     const __half* act;      // [P][I]
     const float* act_scale; // [P][I/64]
@@ -85,6 +97,9 @@ struct PrefillWeights {
     const float *sg, *su, *sd;        // FP8
     const uint8_t *sfg, *sfu, *sfd;   // NVFP4
     float s2g, s2u, s2d;              // NVFP4
+    // NVFP4 with one scale_2 per expert and projection (null: the scalars above)
+    const float *s2g_e, *s2u_e, *s2d_e;
+    int s2_stride;
 };
 cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I, int E, int topk,
                            const int32_t* ids, const float* wts, const PrefillWeights& wt, float limit,

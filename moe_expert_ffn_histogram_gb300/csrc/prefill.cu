@@ -305,6 +305,9 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     gu.sf1 = wt.sfu;
     gu.s2_0 = wt.s2g;
     gu.s2_1 = wt.s2u;
+    gu.s2e_0 = wt.s2g_e;
+    gu.s2e_1 = wt.s2u_e;
+    gu.s2_stride = wt.s2_stride;
     stage_mark(stream, "gate_up_gemm");
     if ((st = launch_prefill_gemm_tw(0, gu, I, stream)) != cudaSuccess) return st;
 
@@ -332,6 +335,8 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     dn.sf1 = wt.sfd;
     dn.s2_0 = wt.s2d;
     dn.s2_1 = wt.s2d;
+    dn.s2e_0 = wt.s2d_e;
+    dn.s2e_1 = wt.s2d_e;
     dn.out = nullptr;
     dn.y16 = reinterpret_cast<__half*>(f32);
     dn.yexp = reinterpret_cast<int8_t*>(ws + L.yexp);

@@ -57,6 +57,10 @@ struct PrefillGemmArgs {
     const uint8_t* sf0;
     const uint8_t* sf1;
     float s2_0, s2_1;
+    // NVFP4 with one scale_2 per expert (null: s2_0 / s2_1): expert e's is s2e_0[e * s2_stride]
+    const float* s2e_0;
+    const float* s2e_1;
+    int s2_stride;
 };
 
 // (m-tile, n-tile) of work item `tile` in expert-major, n-tile-middle, m-tile-minor order: the

@@ -505,8 +505,8 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 winv0 = weight_prescale(p.s0 + sblk * KB, KB, nullptr);
                 winv1 = KIND == 0 ? weight_prescale(p.s1 + sblk * KB, KB, nullptr) : winv0;
             } else {
-                winv0 = p.s2_0;                            // NVFP4: scale_2 of the projection
-                winv1 = KIND == 0 ? p.s2_1 : winv0;
+                winv0 = scale2_of(p.s2_0, p.s2e_0, p.s2_stride, e);   // NVFP4: the expert's scale_2
+                winv1 = KIND == 0 ? scale2_of(p.s2_1, p.s2e_1, p.s2_stride, e) : winv0;
             }
             if constexpr (KIND == 1) {
                 // y goes out in f16 times 2^g, g from |y[r][j]| <= A_r * sum_i |W[j][i]|: A_r the
@@ -514,9 +514,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 // the clamp), both from the gate/up epilogue - the f16 rounding of a and the fp32
                 // sums stay inside the factor 2 between 2^15 and f16's largest value - and the
                 // weight sum 128 * 448 * (sum of the block's scales) for FP8, K * 6 * 448 *
-                // |scale_2| for NVFP4 (E2M1 <= 6, E4M3 scale bytes <= 448)
+                // |the expert's scale_2| for NVFP4 (E2M1 <= 6, E4M3 scale bytes <= 448)
                 const float wsum = FMT == 0 ? 57344.0f * block_scale_abs_sum(p.s0 + sblk * KB, KB)
-                                            : static_cast<float>(p.K) * 2688.0f * fabsf(p.s2_0);
+                                            : static_cast<float>(p.K) * 2688.0f * fabsf(winv0);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     const int t = 32 * i + lane;

@@ -3,6 +3,8 @@
 Integer outputs (route permutation) must match bit for bit; bf16 outputs must be within relative
 L2 <= 5e-3 and max abs <= 2e-2 * RMS(out) of the oracle's double result.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -374,6 +376,53 @@ def test_prefill_f16_scaling_across_magnitudes(fmt, x_scale, limit):
     if x_scale > 1.0:
         assert np.abs(ref).max() > 65504.0        # y itself leaves f16's range
     check_close(bf16_to_f64(run(wl)), ref, f"{fmt} prefill x*{x_scale} limit {limit}")
+
+
+# ---- NVFP4 with one scale_2 per expert and projection ---------------------------------------------
+
+def _expert_scale2_workload(T, E=12, H=512, I=256, seed=977):
+    bank = inputs.make_nvfp4_bank_expert_scale2(E, H, I, seed, device=DEV)
+    x = inputs.normal_activations(T, H, seed, DEV)
+    ids = inputs.make_routes("uniform", T, E, seed).to(DEV)
+    wts = inputs.softmax_route_weights(T, seed).to(DEV)
+    return inputs.Workload(f"expert_scale2_T{T}", "nvfp4", T, H, I, E, inputs.TOPK, x, ids, wts, bank,
+                           inputs.LIMIT)
+
+
+@pytest.mark.parametrize("T", [1, 4, 12, 64])
+def test_nvfp4_expert_scale2_parity(T):
+    """moe_nvfp4_forward_expert_scale2 through every tier - one token, the fused batch-M kernel,
+    sweeps of <= 8 tokens, the grouped GEMM - against the oracle with the same per-expert
+    values (each expert quantised with its own scale_2)."""
+    wl = _expert_scale2_workload(T)
+    assert len(set(wl.bank.scale2_down.tolist())) > 1
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"nvfp4 per-expert scale_2 T={T}")
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_nvfp4_expert_scale2_table_with_stride(T):
+    """The same values as one [E][3] table (gate, up, down columns; stride 3) give the same bits
+    as three [E] arrays."""
+    wl = _expert_scale2_workload(T)
+    b = wl.bank
+    table = torch.stack([b.scale2_gate, b.scale2_up, b.scale2_down], dim=1).contiguous()
+    ref = run(wl)
+    out = torch.empty_like(ref)
+    E, I, _ = b.w_gate.shape
+    ws = torch.empty(int(capi.load().moe_workspace_bytes(T, wl.H, I, E, wl.topk, capi.FMT_NVFP4)),
+                     dtype=torch.uint8, device=DEV)
+    col = lambda j: ctypes.c_void_p(table.data_ptr() + 4 * j)  # noqa: E731
+    rc = capi.load().moe_nvfp4_forward_expert_scale2(
+        ctypes.c_void_p(wl.x.data_ptr()), T, wl.H, I, E, wl.topk, ctypes.c_void_p(wl.ids.data_ptr()),
+        ctypes.c_void_p(wl.wts.data_ptr()), ctypes.c_void_p(b.w_gate.data_ptr()),
+        ctypes.c_void_p(b.sf_gate.data_ptr()), col(0), ctypes.c_void_p(b.w_up.data_ptr()),
+        ctypes.c_void_p(b.sf_up.data_ptr()), col(1), ctypes.c_void_p(b.w_down.data_ptr()),
+        ctypes.c_void_p(b.sf_down.data_ptr()), col(2), 3, wl.limit, ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), None,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
 # ---- bounded waits and buffer bounds -----------------------------------------------------------------

@@ -178,6 +178,29 @@ def alg_bytes(wl):
                 total=w_gu + w_d + x + out + idw, weights=w_gu + w_d)
 
 
+def sweep_rows(T, per=8):
+    """Token counts of the even sweeps of <= per tokens the narrow tiers split T into (never a
+    trailing sweep of one), the split the library makes."""
+    n = (T + per - 1) // per
+    rows, start = [], 0
+    for i in range(n):
+        r = (T - start + (n - i) - 1) // (n - i)
+        rows.append(r)
+        start += r
+    return rows
+
+
+def sweeps_alg_bytes(wl):
+    """Per call of the sweep tier: each sweep reads its own union of selected experts once."""
+    ids = wl.ids.cpu().numpy()
+    total, start = 0, 0
+    for r in sweep_rows(wl.T):
+        distinct = len({int(e) for e in ids[start:start + r].reshape(-1) if 0 <= e < wl.E})
+        total += distinct * (2 * matrix_bytes(wl.fmt, wl.I, wl.H) + matrix_bytes(wl.fmt, wl.H, wl.I))
+        start += r
+    return total + 2 * wl.T * wl.H * 2 + wl.T * wl.topk * 8
+
+
 def kernel_source_sha(files=None):
     """Hash of the kernel's sources: the listed csrc files (its translation unit and the headers
     it includes), or every .cu/.cuh file of csrc when no list is given."""
@@ -564,6 +587,16 @@ def measure_workload(name, args, dev, bank, world, peak, peak_kind, tpeak, want_
                 "note": "step = barrier memset + the fused kernel (CUDA events); bytes over the "
                         "realised union of each route set"}
         launches_per_step = 1
+    elif "gate_up_gemm" not in prefill_stage_ms:
+        # T > 8 below the grouped tier's crossover: ceil(T/8) sweeps through the fused kernel
+        sb = statistics.mean(sweeps_alg_bytes(s_) for s_ in sets)
+        ach = sb / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "fused_forward_kernel (sweeps of <= 8 tokens)",
+                "achieved": round(ach, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": None, "alg_bytes_per_launch": int(sb),
+                "avg_launch_us": round(ms * 1e3, 2),
+                "note": "step = the sweeps (CUDA events); bytes: each sweep's union of experts"}
+        launches_per_step = len(sweep_rows(T))
     else:
         # dominant kernel: the gate/up grouped GEMM (two thirds of the flops), timed by the
         # library's stage events; every (token, slot) pair is one GEMM row
@@ -596,9 +629,10 @@ def measure_workload(name, args, dev, bank, world, peak, peak_kind, tpeak, want_
                            "target_frac": 0.5},
                 "note": "f16 x f16 -> f32 MMA (same nominal rate as bf16); kernel times from the "
                         "library's stage events on the launching stream"}
-        # route plan (three launches from 4096 pairs on), tile list, x prep, gate/up GEMM,
-        # activation prep (only without a clamp limit <= 255), down GEMM, combine
-        launches_per_step = ((3 if P >= 4096 else 1) + 5
+        # route plan and tile list (three launches from 4096 pairs on, the middle one building the
+        # tile list; else two), x prep, gate/up GEMM, activation prep (only without a clamp limit
+        # <= 255), down GEMM, combine
+        launches_per_step = ((3 if P >= 4096 else 2) + 4
                              + (0 if math.isfinite(inputs.LIMIT) and inputs.LIMIT <= 255 else 1))
 
     return {

@@ -127,14 +127,16 @@ MOE_API int moe_route_permute(const int32_t* topk_ids, int T, int topk, int E, i
  * its block scale times a power of two in f16, one rounding per weight; the GEMV tiers apply the
  * scale in fp32), activations are carried as f16 with a power-of-two scale per token (and per
  * 64-wide block of the activation a in the GEMV tiers; per sorted row in the grouped-GEMM tier,
- * or none there when a clamp limit <= 255 bounds |a| by limit^2), products accumulate in fp32,
- * the combine runs in slot order in fp32, and the result is rounded once to bf16.
+ * or one fixed power of two there when a clamp limit <= 255 bounds |a| by limit^2), products
+ * accumulate in fp32, the grouped-GEMM tier keeps each pair's down output in f16 times a power of
+ * two chosen from a bound on it, the combine runs in slot order in fp32, and the result is
+ * rounded once to bf16.
  *
  * Tiers (chosen from the sizes alone): T == 1 two kernels; 2 <= T <= 8 one cooperative kernel;
- * larger T, below the measured crossover (T < 28 FP8, T < 18 NVFP4), the cooperative kernel in
- * even sweeps of <= 8 rows; from it on, the grouped GEMM over expert-sorted rows on the tcgen05
- * tensor cores (H, I <= 8192, E <= 4096; the workspace then holds the sorted rows, about
- * P*(2H + 2I + 4*max(H,I)) bytes for P = T*topk).
+ * larger T the grouped GEMM over expert-sorted rows on the tcgen05 tensor cores (measured faster
+ * than sweeps of <= 8 rows from T = 9 on) when it covers the shape - H, I <= 8192, E <= 4096 -
+ * the workspace then holding the sorted rows, about P*(2H + 2I + 4*max(H,I)) bytes for
+ * P = T*topk; otherwise the cooperative kernel in even sweeps of <= 8 rows.
  */
 MOE_API int moe_fp8_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
                     const int32_t* topk_ids, const float* topk_weights,

@@ -48,13 +48,14 @@ int rows_per_sweep(int T) { return T < kMaxRowsPerSweep ? T : kMaxRowsPerSweep; 
 
 // The grouped-GEMM (prefill) tier: more than one 8-token sweep, and shapes its tiles cover
 // (per-K-block scale tables of <= 64 entries). Smallest T the grouped-GEMM tier takes; below it,
-// sweeps of <= 8 tokens through the cooperative kernel. Measured on GB300 with the decode banks (uniform routes over 256 / 160 experts, L2
-// flushed): FP8 sweeps win up to T = 24 (1.57 vs 1.69 ms) and lose from T = 32 (2.11 vs
-// 2.02 ms); NVFP4 sweeps win at T = 16 (0.57 vs 0.60 ms) and lose from T = 24 (0.86 vs 0.76 ms).
+// sweeps of <= 8 tokens through the cooperative kernel. Measured on GB300 with the decode banks
+// (uniform routes over 256 / 160 experts, L2 flushed): the grouped tier wins from the first width
+// past one sweep - FP8 T = 9: 0.549 vs 0.561 ms, T = 24: 1.16 vs 1.38 ms; NVFP4 T = 9: 0.32 vs
+// 0.38 ms, T = 16: 0.46 vs 0.58 ms - so every T > 8 that it covers goes to it.
 #ifndef MOE_PREFILL_MIN_T
 #define MOE_PREFILL_MIN_T 0
 #endif
-constexpr int kGroupedMinRowsFp8 = 28, kGroupedMinRowsFp4 = 18;
+constexpr int kGroupedMinRowsFp8 = 9, kGroupedMinRowsFp4 = 9;
 
 bool uses_prefill(int T, int H, int I, int E, int fmt) {
     const int min_t = MOE_PREFILL_MIN_T > 0 ? MOE_PREFILL_MIN_T : (fmt == 0 ? kGroupedMinRowsFp8 : kGroupedMinRowsFp4);

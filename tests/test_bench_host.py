@@ -120,3 +120,14 @@ def test_graded_fraction_takes_the_larger_floor():
     assert abs(floor - 1e-3) < 1e-9 and abs(f - 0.5) < 1e-9
     f, floor = bench.graded_fraction(13.5468e9, 1.93e12, 4e-3, 6773.4, 1930.0)   # bytes dominate
     assert abs(floor - 2e-3) < 1e-9 and abs(f - 0.5) < 1e-9
+
+
+def test_sweep_rows_even_split():
+    """The narrow tiers' split of T tokens into ceil(T/8) even sweeps, never a trailing sweep of
+    one (forward.rs, `moe_row_groups`), as bench.py models it."""
+    assert bench.sweep_rows(9) == [5, 4]
+    assert bench.sweep_rows(16) == [8, 8]
+    assert bench.sweep_rows(17) == [6, 6, 5]
+    for T in range(1, 300):
+        r = bench.sweep_rows(T)
+        assert sum(r) == T and len(r) == (T + 7) // 8 and max(r) - min(r) <= 1 and max(r) <= 8

@@ -321,11 +321,14 @@ def test_nvfp4_prefill_full_size_sampled():
     check_close(bf16_to_f64(out[toks]), res["out"], f"nvfp4_prefill on {len(toks)} sampled tokens")
 
 
-@pytest.mark.parametrize("fmt,T", [("fp8", 27), ("fp8", 28), ("nvfp4", 17), ("nvfp4", 18)])
-def test_tier_crossover_both_sides(fmt, T):
-    """Just below (8-token sweeps) and at (grouped GEMM) the measured crossover width."""
-    wl = inputs.make_custom(fmt, T, 512, 256, 20, seed=950 + T, device=DEV)
-    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"crossover {fmt} T={T}")
+@pytest.mark.parametrize("fmt,T,H,I", [("fp8", 8, 512, 256), ("fp8", 9, 512, 256), ("nvfp4", 8, 512, 256),
+                                       ("nvfp4", 9, 512, 256), ("nvfp4", 9, 384, 256), ("nvfp4", 20, 512, 128)])
+def test_tier_crossover_both_sides(fmt, T, H, I):
+    """Both sides of the measured crossover: T = 8 (one cooperative sweep) and T = 9 (the grouped
+    GEMM), and NVFP4 shapes the grouped tier does not cover (H or I not a multiple of 256), which
+    run as sweeps of <= 8 tokens at any T."""
+    wl = inputs.make_custom(fmt, T, H, I, 20, seed=950 + T, device=DEV)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"crossover {fmt} T={T} H={H} I={I}")
 
 
 def test_prefill_bitwise_repeatable():

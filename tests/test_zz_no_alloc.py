@@ -52,8 +52,9 @@ def entry():
 @pytest.mark.parametrize("T", [1, 5, 17])
 def test_noalloc_matches_workspace_entry_point_two_calls(entry, T):
     """Two calls in a row with different inputs; each is bit-identical to moe_fp8_forward with a
-    caller workspace (the same kernels on the same inputs). T = 17 runs three sweeps of <= 8
-    tokens that reuse the scratch regions, the barrier word included, in stream order."""
+    caller workspace (the same kernels on the same inputs). T = 5 runs the cooperative kernel
+    (its barrier word in the scratch), T = 17 the grouped-GEMM tier, whose plan, sorted copies
+    and intermediates fill most of the 1 MiB and are rewritten in stream order by each call."""
     assert capi.workspace_bytes(T, 1024, 512, 16, 8, capi.FMT_FP8) <= SCRATCH_BYTES
     bank = inputs.make_fp8_bank(16, 1024, 512, seed=404, device=DEV)
     for call in range(2):                      # two calls in a row, different inputs

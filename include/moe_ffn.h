@@ -227,6 +227,22 @@ MOE_API int moe_nvfp4_forward_layer(const uint16_t* x, int T, int H, int I, int 
                                     int32_t* err, void* stream);
 
 /*
+ * moe_nvfp4_forward_layer_expert_scale2 - moe_nvfp4_forward_layer with one scale_2 per expert and
+ * projection: the tables, stride and errors of moe_nvfp4_forward_expert_scale2, the shared and
+ * residual inputs and the single-rounding epilogue of moe_nvfp4_forward_layer.
+ */
+MOE_API int moe_nvfp4_forward_layer_expert_scale2(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                                  const int32_t* topk_ids, const float* topk_weights,
+                                                  const uint8_t* w_gate, const uint8_t* sf_gate,
+                                                  const float* scale2_gate, const uint8_t* w_up,
+                                                  const uint8_t* sf_up, const float* scale2_up,
+                                                  const uint8_t* w_down, const uint8_t* sf_down,
+                                                  const float* scale2_down, int scale2_stride, float limit,
+                                                  const uint16_t* shared, const uint16_t* residual,
+                                                  uint16_t* out, void* workspace, size_t workspace_bytes,
+                                                  int32_t* err, void* stream);
+
+/*
  * Stage entry points. moe_plan, then moe_*_gate_up, then moe_*_down_combine (on one stream, same
  * workspace, same arguments as the forward they stand for) compute exactly the bits of
  * moe_*_forward for T <= 8, as three separate kernels; moe_*_forward runs the same work items in

@@ -30,7 +30,7 @@ EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_
             "moe_router_workspace_bytes", "moe_router", "moe_fp8_forward_layer",
             "moe_nvfp4_forward_layer", "moe_shared_expert_workspace_bytes", "moe_shared_expert_bf16",
             "moe_stage_timing", "moe_stage_times", "moe_test_barrier_timeout",
-            "moe_nvfp4_forward_expert_scale2")
+            "moe_nvfp4_forward_expert_scale2", "moe_nvfp4_forward_layer_expert_scale2")
 
 _lib = None
 
@@ -94,6 +94,10 @@ def load(path: Optional[str] = None):
     lib.moe_nvfp4_forward_layer.restype = i32
     lib.moe_nvfp4_forward_layer.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, f32, vp, vp,
                                             f32, vp, vp, f32, f32, vp, vp, vp, vp, sz, vp, vp]
+    lib.moe_nvfp4_forward_layer_expert_scale2.restype = i32
+    lib.moe_nvfp4_forward_layer_expert_scale2.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                                          vp, vp, vp, vp, vp, vp, i32, f32, vp, vp, vp, vp,
+                                                          sz, vp, vp]
     lib.moe_shared_expert_workspace_bytes.restype = sz
     lib.moe_shared_expert_workspace_bytes.argtypes = [i32, i32, i32]
     lib.moe_shared_expert_bf16.restype = i32
@@ -258,8 +262,8 @@ def forward(x, ids, wts, bank, limit: float, **kw):
 
 def forward_layer(x, ids, wts, bank, limit: float, shared=None, residual=None, out=None,
                   workspace=None, err=None, stream=None):
-    """moe_*_forward_layer: the forward with out = bf16((routed + shared) + residual)."""
-    _scalar_scale2_only(bank, "forward_layer")
+    """moe_*_forward_layer: the forward with out = bf16((routed + shared) + residual) (an NVFP4 bank
+    with one scale_2 per expert goes through moe_nvfp4_forward_layer_expert_scale2)."""
     E, I, _ = bank.w_gate.shape
     fmt = FMT_FP8 if bank.fmt == "fp8" else FMT_NVFP4
     dev, T, H, topk, out, ws = _common(x, ids, wts, out, workspace, err, fmt, E, I)
@@ -275,6 +279,19 @@ def forward_layer(x, ids, wts, bank, limit: float, shared=None, residual=None, o
                                        _ptr(bank.s_up), _ptr(bank.w_down), _ptr(bank.s_down),
                                        float(limit), _ptr(shared), _ptr(residual), _ptr(out), _ptr(ws),
                                        ws.numel(), _ptr(err), _stream(dev, stream))
+    elif _per_expert_scale2(bank):
+        for n in ("scale2_gate", "scale2_up", "scale2_down"):
+            t = getattr(bank, n)
+            _need(t, n, torch.float32, dev)
+            if tuple(t.shape) != (E,):
+                raise ValueError(f"{n} must be [E] per expert")
+        rc = lib.moe_nvfp4_forward_layer_expert_scale2(
+            _ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
+            _ptr(bank.w_gate), _ptr(bank.sf_gate), _ptr(bank.scale2_gate),
+            _ptr(bank.w_up), _ptr(bank.sf_up), _ptr(bank.scale2_up),
+            _ptr(bank.w_down), _ptr(bank.sf_down), _ptr(bank.scale2_down), 1,
+            float(limit), _ptr(shared), _ptr(residual), _ptr(out), _ptr(ws), ws.numel(), _ptr(err),
+            _stream(dev, stream))
     else:
         rc = lib.moe_nvfp4_forward_layer(_ptr(x), T, H, I, E, topk, _ptr(ids), _ptr(wts),
                                          _ptr(bank.w_gate), _ptr(bank.sf_gate), float(bank.scale2_gate),

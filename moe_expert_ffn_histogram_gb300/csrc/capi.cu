@@ -478,6 +478,29 @@ int moe_nvfp4_forward_layer(const uint16_t* x, int T, int H, int I, int E, int t
                       workspace_bytes, err, static_cast<cudaStream_t>(stream), shared, residual);
 }
 
+int moe_nvfp4_forward_layer_expert_scale2(const uint16_t* x, int T, int H, int I, int E, int topk,
+                                          const int32_t* topk_ids, const float* topk_weights,
+                                          const uint8_t* w_gate, const uint8_t* sf_gate, const float* scale2_gate,
+                                          const uint8_t* w_up, const uint8_t* sf_up, const float* scale2_up,
+                                          const uint8_t* w_down, const uint8_t* sf_down, const float* scale2_down,
+                                          int scale2_stride, float limit, const uint16_t* shared,
+                                          const uint16_t* residual, uint16_t* out, void* workspace,
+                                          size_t workspace_bytes, int32_t* err, void* stream) {
+    if (!x || !topk_ids || !topk_weights || !w_gate || !sf_gate || !w_up || !sf_up || !w_down ||
+        !sf_down || !out || !scale2_gate || !scale2_up || !scale2_down)
+        return MOE_ERR_NULL;
+    if (!limit_ok(limit) || scale2_stride < 1) return MOE_ERR_VALUE;
+    if (!all_aligned(x, w_gate, w_up, w_down, sf_gate, sf_up, sf_down, out)) return MOE_ERR_ALIGN;
+    if ((shared && !aligned16(shared)) || (residual && !aligned16(residual))) return MOE_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(scale2_gate) | reinterpret_cast<uintptr_t>(scale2_up) |
+         reinterpret_cast<uintptr_t>(scale2_down)) & 3u)
+        return MOE_ERR_ALIGN;
+    return forward<1>(x, T, H, I, E, topk, topk_ids, topk_weights, Proj{w_gate, nullptr, sf_gate, 1.f},
+                      Proj{w_up, nullptr, sf_up, 1.f}, Proj{w_down, nullptr, sf_down, 1.f}, limit, out,
+                      workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream), shared, residual,
+                      ExpertScale2{scale2_gate, scale2_up, scale2_down, scale2_stride});
+}
+
 // ---- stage entry points (T <= 8: one sweep) -------------------------------------------------
 
 int moe_plan(int T, int H, int I, int E, int topk, int fmt, const int32_t* topk_ids,

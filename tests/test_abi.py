@@ -129,6 +129,20 @@ def test_nvfp4_expert_scale2_rejects_bad_arguments(lib):
     assert call(ws_bytes=0) == -3
 
 
+def test_nvfp4_layer_expert_scale2_rejects_bad_arguments(lib):
+    def call(**over):
+        a = dict(x=FAKE, T=1, H=256, I=128, E=16, topk=8, ids=FAKE, wts=FAKE, wg=FAKE, sfg=FAKE,
+                 s2g=FAKE, wu=FAKE, sfu=FAKE, s2u=FAKE, wd=FAKE, sfd=FAKE, s2d=FAKE, stride=3,
+                 limit=7.0, shared=None, residual=None, out=FAKE, ws=FAKE, ws_bytes=1 << 30, err=None,
+                 stream=None)
+        a.update(over)
+        return lib.moe_nvfp4_forward_layer_expert_scale2(*a.values())
+    assert call(s2g=None) == -1
+    assert call(stride=-1) == -4
+    assert call(shared=ctypes.c_void_p(FAKE.value + 8)) == -7
+    assert call(ws_bytes=0) == -3
+
+
 def test_route_permute_rejects_bad_arguments(lib):
     f = lib.moe_route_permute
     assert f(None, 1, 8, 16, FAKE, FAKE, FAKE, FAKE, None, None) == -1

@@ -40,6 +40,29 @@ def test_layer_epilogue_parity(fmt, T, H, I, E):
                        capi.forward(wl.x, wl.ids, wl.wts, wl.bank, wl.limit).view(torch.int16))
 
 
+@pytest.mark.parametrize("T", [1, 5, 40])
+def test_layer_epilogue_with_expert_scale2(T):
+    """moe_nvfp4_forward_layer_expert_scale2: one scale_2 per expert and projection, with the shared
+    expert and the residual in the combine, on the single-token, fused and grouped tiers."""
+    E, H, I = 10, 512, 256
+    bank = inputs.make_nvfp4_bank_expert_scale2(E, H, I, seed=310 + T, device=DEV)
+    x = inputs.normal_activations(T, H, 310 + T, DEV)
+    ids = inputs.make_routes("uniform", T, E, 310 + T).to(DEV)
+    wts = inputs.softmax_route_weights(T, 310 + T).to(DEV)
+    wl = inputs.Workload(f"layer_s2_T{T}", "nvfp4", T, H, I, E, inputs.TOPK, x, ids, wts, bank, inputs.LIMIT)
+    shared = _rand_bf16((T, H), 311 + T, 0.05)
+    resid = _rand_bf16((T, H), 312 + T, 1.0)
+    out = capi.forward_layer(wl.x, wl.ids, wl.wts, bank, wl.limit, shared=shared, residual=resid)
+    plain = capi.forward_layer(wl.x, wl.ids, wl.wts, bank, wl.limit)
+    torch.cuda.synchronize()
+    ref = oracle_for(wl)
+    _, ref_b = oracle.layer_epilogue(ref["out"], _bits(shared), _bits(resid))
+    want = np.array([oracle.bf16_value(int(v)) for v in ref_b.reshape(-1)]).reshape(ref_b.shape)
+    check_close(bf16_to_f64(out), want, f"layer per-expert scale_2 T={T}")
+    assert torch.equal(plain.view(torch.int16),
+                       capi.forward(wl.x, wl.ids, wl.wts, bank, wl.limit).view(torch.int16))
+
+
 @pytest.mark.parametrize("T,H,S", [(1, 512, 256), (7, 256, 512), (100, 512, 256)])
 def test_shared_expert_parity(T, H, S):
     x = _rand_bf16((T, H), 400 + T)

@@ -402,6 +402,29 @@ def test_nvfp4_expert_scale2_parity(T):
     check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"nvfp4 per-expert scale_2 T={T}")
 
 
+@pytest.mark.parametrize("T", [1, 6, 64])
+def test_nvfp4_expert_scale2_zero_and_negative(T):
+    """Per-expert values of 0 (an expert that contributes nothing) and of a negative sign (its
+    outputs flip) on every tier; the grouped tier's f16 bound for y uses |scale_2|."""
+    wl = _expert_scale2_workload(T, seed=978)
+    b = wl.bank
+    for t in (b.scale2_gate, b.scale2_up, b.scale2_down):
+        t[3] = 0.0
+        t[5] = -t[5]
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"nvfp4 scale_2 zero/negative T={T}")
+
+
+def test_prefill_zero_token_rows():
+    """Tokens whose x is all zero: their activation rows (and, when every token of an m-tile is zero,
+    the m-tile maximum) are 0, so y's power of two falls back to 1 and their outputs are exactly 0."""
+    wl = inputs.make_custom("fp8", 40, 256, 256, 10, seed=979, device=DEV)
+    wl.x[3].zero_()
+    wl.x[17].zero_()
+    out = run(wl)
+    assert torch.count_nonzero(out[3]) == 0 and torch.count_nonzero(out[17]) == 0
+    check_close(bf16_to_f64(out), oracle_for(wl)["out"], "prefill zero tokens")
+
+
 @pytest.mark.parametrize("T", [1, 64])
 def test_nvfp4_expert_scale2_table_with_stride(T):
     """The same values as one [E][3] table (gate, up, down columns; stride 3) give the same bits

@@ -414,6 +414,15 @@ def test_nvfp4_expert_scale2_zero_and_negative(T):
     check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"nvfp4 scale_2 zero/negative T={T}")
 
 
+@pytest.mark.parametrize("fmt,E", [("fp8", 4096), ("nvfp4", 1024)])
+def test_grouped_tier_many_experts_few_tokens(fmt, E):
+    """The grouped tier at its smallest width (T = 9) over a bank with thousands of experts: the
+    route plan, the m-tile list (almost every expert empty) and the GEMMs' tile decode."""
+    H, I = (256, 128) if fmt == "fp8" else (256, 256)
+    wl = inputs.make_custom(fmt, 9, H, I, E, seed=981, device=DEV)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"{fmt} grouped T=9 E={E}")
+
+
 def test_prefill_zero_token_rows():
     """Tokens whose x is all zero: their activation rows (and, when every token of an m-tile is zero,
     the m-tile maximum) are 0, so y's power of two falls back to 1 and their outputs are exactly 0."""

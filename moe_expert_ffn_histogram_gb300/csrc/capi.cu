@@ -355,6 +355,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 template <class... P>
 bool all_aligned(const P*... p) { return (aligned16(p) && ...); }
 
+// The per-expert scale_2 tables: present, 4-byte aligned, a stride of at least one element.
+int check_expert_scale2(const ExpertScale2& t) {
+    if (!t.g || !t.u || !t.d) return MOE_ERR_NULL;
+    if (t.stride < 1) return MOE_ERR_VALUE;
+    if ((reinterpret_cast<uintptr_t>(t.g) | reinterpret_cast<uintptr_t>(t.u) | reinterpret_cast<uintptr_t>(t.d)) & 3u)
+        return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -423,17 +432,15 @@ int moe_nvfp4_forward_expert_scale2(const uint16_t* x, int T, int H, int I, int 
                                     int scale2_stride, float limit, uint16_t* out, void* workspace,
                                     size_t workspace_bytes, int32_t* err, void* stream) {
     if (!x || !topk_ids || !topk_weights || !w_gate || !sf_gate || !w_up || !sf_up || !w_down ||
-        !sf_down || !out || !scale2_gate || !scale2_up || !scale2_down)
+        !sf_down || !out)
         return MOE_ERR_NULL;
-    if (!limit_ok(limit) || scale2_stride < 1) return MOE_ERR_VALUE;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
     if (!all_aligned(x, w_gate, w_up, w_down, sf_gate, sf_up, sf_down, out)) return MOE_ERR_ALIGN;
-    if ((reinterpret_cast<uintptr_t>(scale2_gate) | reinterpret_cast<uintptr_t>(scale2_up) |
-         reinterpret_cast<uintptr_t>(scale2_down)) & 3u)
-        return MOE_ERR_ALIGN;
+    const ExpertScale2 xs2{scale2_gate, scale2_up, scale2_down, scale2_stride};
+    if (const int rc = check_expert_scale2(xs2)) return rc;
     return forward<1>(x, T, H, I, E, topk, topk_ids, topk_weights, Proj{w_gate, nullptr, sf_gate, 1.f},
                       Proj{w_up, nullptr, sf_up, 1.f}, Proj{w_down, nullptr, sf_down, 1.f}, limit, out,
-                      workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream), nullptr, nullptr,
-                      ExpertScale2{scale2_gate, scale2_up, scale2_down, scale2_stride});
+                      workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream), nullptr, nullptr, xs2);
 }
 
 // ---- the forwards with the layer epilogue ---------------------------------------------------
@@ -487,18 +494,16 @@ int moe_nvfp4_forward_layer_expert_scale2(const uint16_t* x, int T, int H, int I
                                           const uint16_t* residual, uint16_t* out, void* workspace,
                                           size_t workspace_bytes, int32_t* err, void* stream) {
     if (!x || !topk_ids || !topk_weights || !w_gate || !sf_gate || !w_up || !sf_up || !w_down ||
-        !sf_down || !out || !scale2_gate || !scale2_up || !scale2_down)
+        !sf_down || !out)
         return MOE_ERR_NULL;
-    if (!limit_ok(limit) || scale2_stride < 1) return MOE_ERR_VALUE;
+    if (!limit_ok(limit)) return MOE_ERR_VALUE;
     if (!all_aligned(x, w_gate, w_up, w_down, sf_gate, sf_up, sf_down, out)) return MOE_ERR_ALIGN;
     if ((shared && !aligned16(shared)) || (residual && !aligned16(residual))) return MOE_ERR_ALIGN;
-    if ((reinterpret_cast<uintptr_t>(scale2_gate) | reinterpret_cast<uintptr_t>(scale2_up) |
-         reinterpret_cast<uintptr_t>(scale2_down)) & 3u)
-        return MOE_ERR_ALIGN;
+    const ExpertScale2 xs2{scale2_gate, scale2_up, scale2_down, scale2_stride};
+    if (const int rc = check_expert_scale2(xs2)) return rc;
     return forward<1>(x, T, H, I, E, topk, topk_ids, topk_weights, Proj{w_gate, nullptr, sf_gate, 1.f},
                       Proj{w_up, nullptr, sf_up, 1.f}, Proj{w_down, nullptr, sf_down, 1.f}, limit, out,
-                      workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream), shared, residual,
-                      ExpertScale2{scale2_gate, scale2_up, scale2_down, scale2_stride});
+                      workspace, workspace_bytes, err, static_cast<cudaStream_t>(stream), shared, residual, xs2);
 }
 
 // ---- stage entry points (T <= 8: one sweep) -------------------------------------------------

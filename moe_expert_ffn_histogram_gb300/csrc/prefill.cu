@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(256) prefill_x_prep_kernel(const __nv_bfloat16
     for (int w = 0; w < 8; ++w) mm = fmaxf(mm, red[w]);
     float inv;
     const float s = pow2_range_scale(mm, inv);
+    pdl_wait();                        // the route plan's pair_to_sorted (programmatic dependent launch)
     if (tid == 0) xinv[t] = inv;
     const int ncopy = pair_to_sorted != nullptr ? topk : 1;
     for (int v = tid; v < nv; v += 256) {
@@ -233,6 +234,23 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     cudaError_t st;
     const TileList tl{I32(L.tiles), I32(L.tile_e), I32(L.tile_r0), I32(L.tile_first), I32(L.tile_cnt),
                       prefill::kBM};
+    uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
+    // a finite clamp limit L <= 255 bounds |a| = |silu(min(g, L)) * clamp(u, -L, L)| by L^2, which
+    // f16 holds without a range scale: the TMEM core then writes a in f16 itself
+    const bool a16_direct = std::isfinite(limit) && limit <= kA16DirectLimit;
+    // the direct f16 activations carry one power of two 2^s with L^2 * 2^s < 2^15, so that small
+    // activations stay clear of f16's subnormal range
+    int l2e = 0;
+    if (a16_direct) std::frexp(static_cast<double>(limit) * limit, &l2e);
+    const int a16_s = a16_direct && limit > 0.0f ? 15 - l2e : 0;
+    // max |a| per sorted row (range-scaled activations: their scale, and y's f16 factor) or per
+    // m-tile (f16 activations under the clamp: y's f16 factor); zeroed before the route plan, so
+    // that the plan kernels, x prep and the gate/up GEMM follow one another as programmatic
+    // dependent launches
+    uint32_t* tmax = reinterpret_cast<uint32_t*>(ws + L.tmax);
+    if (!a16_direct && (st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess)
+        return st;
+    if (a16_direct && (st = cudaMemsetAsync(tmax, 0, L.yexp - L.tmax, stream)) != cudaSuccess) return st;
     stage_mark(stream, "route_plan");
     // many pairs: the multi-block plan (one block serialises ~32 rounds of 1024 pairs), which also
     // builds the m-tile list
@@ -248,28 +266,24 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
         prefill_tiles_kernel<<<1, 1024, 0, stream>>>(I32(L.counts), I32(L.offsets), E, tl);
         if ((st = cudaGetLastError()) != cudaSuccess) return st;
     }
-    uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);
-    // a finite clamp limit L <= 255 bounds |a| = |silu(min(g, L)) * clamp(u, -L, L)| by L^2, which
-    // f16 holds without a range scale: the TMEM core then writes a in f16 itself
-    const bool a16_direct = std::isfinite(limit) && limit <= kA16DirectLimit;
-    // the direct f16 activations carry one power of two 2^s with L^2 * 2^s < 2^15, so that small
-    // activations stay clear of f16's subnormal range
-    int l2e = 0;
-    if (a16_direct) std::frexp(static_cast<double>(limit) * limit, &l2e);
-    const int a16_s = a16_direct && limit > 0.0f ? 15 - l2e : 0;
-    // max |a| per sorted row (range-scaled activations: their scale, and y's f16 factor) or per
-    // m-tile (f16 activations under the clamp: y's f16 factor); zeroed before x prep, so that the
-    // gate/up GEMM follows x prep directly (programmatic dependent launch)
-    uint32_t* tmax = reinterpret_cast<uint32_t*>(ws + L.tmax);
-    if (!a16_direct && (st = cudaMemsetAsync(amax, 0, static_cast<size_t>(P) * 4, stream)) != cudaSuccess)
-        return st;
-    if (a16_direct && (st = cudaMemsetAsync(tmax, 0, L.yexp - L.tmax, stream)) != cudaSuccess) return st;
     __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
     float* xinv = reinterpret_cast<float*>(ws + L.xinv);
     stage_mark(stream, "x_prep");
-    prefill_x_prep_kernel<<<T, 256, 0, stream>>>(x, H, x16, xinv,
-                                                  I32(L.pair_to_sorted), topk);
-    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    {
+        // a programmatic dependent of the last plan kernel: x's range scales overlap its tail
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(T);
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((st = cudaLaunchKernelEx(&cfg, prefill_x_prep_kernel, x, H, x16, xinv,
+                                     static_cast<const int32_t*>(I32(L.pair_to_sorted)), topk)) != cudaSuccess)
+            return st;
+    }
 
     float* f32 = reinterpret_cast<float*>(ws + L.f32);
     PrefillGemmArgs gu{};

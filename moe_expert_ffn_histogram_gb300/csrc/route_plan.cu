@@ -164,6 +164,7 @@ plan_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restr
     extern __shared__ __align__(16) int smem_i[];
     int* cnt = smem_i;                 // [E]
     const int tid = threadIdx.x;
+    pdl_launch_dependents();           // the base kernel may start; it waits for this grid
     for (int e = tid; e < E; e += kPlanThreads) cnt[e] = 0;
     __syncthreads();
     const int p = blockIdx.x * kPlanThreads + tid;
@@ -191,6 +192,8 @@ plan_base_kernel(int P, int E, int nblk, int32_t* __restrict__ blk, int32_t* __r
     __shared__ int scratch[33];
     const int tid = threadIdx.x;
     const size_t nall = static_cast<size_t>(nblk) * E;
+    pdl_wait();                        // the histogram grid's counts (programmatic dependent launch)
+    pdl_launch_dependents();
     if (staged) {
         for (size_t i = tid; i < nall; i += kPlanThreads) bc[i] = blk[i];
         __syncthreads();
@@ -230,6 +233,8 @@ plan_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t
     extern __shared__ __align__(16) int smem_i[];
     uint8_t* pre = reinterpret_cast<uint8_t*>(smem_i);   // [32][E] per-warp counts
     const int tid = threadIdx.x, warp = tid >> 5;
+    pdl_wait();                        // the base kernel's block bases (programmatic dependent launch)
+    pdl_launch_dependents();
     for (int i = tid; i < 32 * E; i += kPlanThreads) pre[i] = 0;
     __syncthreads();
     const int p = blockIdx.x * kPlanThreads + tid;
@@ -275,9 +280,28 @@ cudaError_t launch_route_plan_wide(const int32_t* ids, int P, int E, int32_t* co
             if (st != cudaSuccess) return st;
         }
     plan_hist_kernel<<<nblk, kPlanThreads, s1, stream>>>(ids, P, E, blk, err);
-    plan_base_kernel<<<1, kPlanThreads, s2, stream>>>(P, E, nblk, blk, counts, offsets, sorted_pair,
-                                                      staged ? 1 : 0, tl);
-    plan_scatter_kernel<<<nblk, kPlanThreads, s3, stream>>>(ids, P, E, blk, sorted_pair, pair_to_sorted);
+    cudaError_t st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+    // the base and scatter kernels are programmatic dependents of the kernel before them: each
+    // is resident and waiting (griddepcontrol.wait) when its predecessor completes
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(1);
+    cfg.dynamicSmemBytes = s2;
+    if ((st = cudaLaunchKernelEx(&cfg, plan_base_kernel, P, E, nblk, blk, counts, offsets, sorted_pair,
+                                 staged ? 1 : 0, tl)) != cudaSuccess)
+        return st;
+    cfg.gridDim = dim3(nblk);
+    cfg.dynamicSmemBytes = s3;
+    if ((st = cudaLaunchKernelEx(&cfg, plan_scatter_kernel, ids, P, E, static_cast<const int32_t*>(blk),
+                                 sorted_pair, pair_to_sorted)) != cudaSuccess)
+        return st;
     return cudaGetLastError();
 }
 

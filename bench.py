@@ -301,6 +301,44 @@ def hold_stream():
     torch.cuda._sleep(HOLD_CYCLES)
 
 
+def stream_ceiling_us(nbytes, dev, flush, reps):
+    """Median device time (us) of one plain streaming-read kernel (moe_stream_read) over nbytes,
+    timed like a forward step: L2 flushed, stream held, CUDA events around the launch. What one
+    kernel of that many bytes reaches on the device, the ceiling a step of the same bytes is read
+    against (launch latency and the ramp at either end weigh more the fewer bytes a call moves)."""
+    from moe_expert_ffn_histogram_gb300 import capi
+    n = int(nbytes) // 16 * 16
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ts = []
+    for i in range(3 + reps):
+        flush.zero_()
+        hold_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        capi.stream_read(buf, n, sink)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            ts.append(a.elapsed_time(b) * 1e3)
+    del buf
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def ceiling_entry(nbytes, t_us, ceil_us, peak, key):
+    """One stream_ceiling entry: the plain read of the same bytes, and how the timed work compares."""
+    gbs = nbytes / (ceil_us * 1e-6) / 1e9
+    return {"bytes": int(nbytes), "read_us": round(ceil_us, 2), "read_gbs": round(gbs, 1),
+            "read_frac_of_peak": round(gbs / peak, 4), key: round(ceil_us / t_us, 4)}
+
+
+CEILING_RULE = ("one plain streaming-read kernel (moe_stream_read) over the same number of "
+                "algorithmic bytes, timed like the step (L2 flushed, CUDA events around the launch, "
+                "median); *_vs_read = read time / measured time (1.0: as fast as a plain read)")
+
+
 # ---- harness statistics ---------------------------------------------------------------------------
 
 def nearest_rank(sorted_vals, percentile: int):
@@ -577,6 +615,15 @@ def measure_workload(name, args, dev, bank, world, peak, peak_kind, tpeak, want_
                          "alg_bytes": int(mean_total), "achieved": round(call_gbs, 1),
                          "frac": round(call_gbs / peak, 4)},
                 "note": "CUDA events on the launching stream"}
+        reps = max(args.steps, 10)
+        roof["stream_ceiling"] = {
+            "rule": CEILING_RULE,
+            "step": ceiling_entry(mean_total, ms * 1e3, stream_ceiling_us(mean_total, dev, flush, reps),
+                                  peak, "step_vs_read"),
+            "gate_up": ceiling_entry(gu_bytes, gu_ms * 1e3, stream_ceiling_us(gu_bytes, dev, flush, reps),
+                                     peak, "kernel_vs_read"),
+            "down": ceiling_entry(dn_bytes, dn_ms * 1e3, stream_ceiling_us(dn_bytes, dev, flush, reps),
+                                  peak, "kernel_vs_read")}
         launches_per_step = 2
     elif T <= 8:
         ach = mean_total / (ms * 1e-3) / 1e9
@@ -586,6 +633,11 @@ def measure_workload(name, args, dev, bank, world, peak, peak_kind, tpeak, want_
                 "avg_launch_us": round(ms * 1e3, 2),
                 "note": "step = barrier memset + the fused kernel (CUDA events); bytes over the "
                         "realised union of each route set"}
+        roof["stream_ceiling"] = {
+            "rule": CEILING_RULE,
+            "step": ceiling_entry(mean_total, ms * 1e3,
+                                  stream_ceiling_us(mean_total, dev, flush, max(args.steps, 10)),
+                                  peak, "step_vs_read")}
         launches_per_step = 1
     elif "gate_up_gemm" not in prefill_stage_ms:
         # T > 8 below the grouped tier's crossover: ceil(T/8) sweeps through the fused kernel

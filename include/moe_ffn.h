@@ -378,6 +378,23 @@ MOE_API int moe_stage_times(float* ms, const char** names, int max_stages);
  */
 MOE_API int moe_test_barrier_timeout(int enable);
 
+/*
+ * moe_stream_read - measurement aid, not part of the forward. Reads the device buffer
+ * [buf, buf + bytes) once with one plain streaming kernel (16-byte loads, consecutive threads on
+ * consecutive words, two 512-thread blocks per SM) and XORs every 32-bit word of it into *sink
+ * (device memory; not cleared by the library, so the caller zeroes it first; the fold does not
+ * depend on the order of the blocks). What this kernel reaches on a given byte count, timed the
+ * way a forward is timed, is the read throughput one kernel of that size gets from HBM on the
+ * device: launch latency and the ramp at either end weigh more the fewer bytes a call moves, so
+ * the fraction of the peak copy bandwidth a forward can reach depends on its size. The benchmark
+ * reports it beside each bandwidth-bound workload's fraction.
+ *   buf    device pointer, 16-byte aligned (MOE_ERR_ALIGN), read only.
+ *   bytes  a positive multiple of 16 (MOE_ERR_SHAPE otherwise).
+ *   sink   device pointer to one uint32_t, 4-byte aligned.
+ * Returns MOE_OK, MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN or MOE_ERR_CUDA. One launch.
+ */
+MOE_API int moe_stream_read(const void* buf, size_t bytes, uint32_t* sink, void* stream);
+
 /* Library build identification: the compiled CUDA architecture string (e.g. "sm_103a"). */
 MOE_API const char* moe_build_arch(void);
 

@@ -30,7 +30,8 @@ EXPORTED = ("moe_workspace_bytes", "moe_route_permute", "moe_fp8_forward", "moe_
             "moe_router_workspace_bytes", "moe_router", "moe_fp8_forward_layer",
             "moe_nvfp4_forward_layer", "moe_shared_expert_workspace_bytes", "moe_shared_expert_bf16",
             "moe_stage_timing", "moe_stage_times", "moe_test_barrier_timeout",
-            "moe_nvfp4_forward_expert_scale2", "moe_nvfp4_forward_layer_expert_scale2")
+            "moe_nvfp4_forward_expert_scale2", "moe_nvfp4_forward_layer_expert_scale2",
+            "moe_stream_read")
 
 _lib = None
 
@@ -106,6 +107,8 @@ def load(path: Optional[str] = None):
     lib.moe_stage_timing.argtypes = [i32]
     lib.moe_test_barrier_timeout.restype = i32
     lib.moe_test_barrier_timeout.argtypes = [i32]
+    lib.moe_stream_read.restype = i32
+    lib.moe_stream_read.argtypes = [vp, sz, vp, vp]
     lib.moe_stage_times.restype = i32
     lib.moe_stage_times.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), i32]
     if path is None:
@@ -376,6 +379,19 @@ def down_combine(ids, wts, bank, out, workspace, stream=None):
 def test_barrier_timeout(enable: bool) -> None:
     """moe_test_barrier_timeout: make the cooperative forward's grid barrier time out (test hook)."""
     _check("moe_test_barrier_timeout", load().moe_test_barrier_timeout(1 if enable else 0))
+
+
+def stream_read(buf: torch.Tensor, nbytes: int, sink: torch.Tensor, stream=None) -> None:
+    """moe_stream_read: one plain streaming read of the first nbytes of buf (a device tensor),
+    every 32-bit word XORed into sink (an int32 tensor of one element, not cleared). A
+    measurement aid: the read throughput one kernel of nbytes reaches on the device."""
+    if not isinstance(buf, torch.Tensor) or not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    if nbytes > buf.numel() * buf.element_size():
+        raise ValueError("nbytes exceeds the buffer")
+    _need(sink, "sink", torch.int32, buf.device)
+    _check("moe_stream_read", load().moe_stream_read(_ptr(buf), int(nbytes), _ptr(sink),
+                                                      _stream(buf.device, stream)))
 
 
 def build_arch() -> str:

@@ -661,6 +661,15 @@ int moe_shared_expert_bf16(const uint16_t* x, int T, int H, int S, const uint16_
         static_cast<cudaStream_t>(stream)));
 }
 
+int moe_stream_read(const void* buf, size_t bytes, uint32_t* sink, void* stream) {
+    if (buf == nullptr || sink == nullptr) return MOE_ERR_NULL;
+    if (bytes == 0 || bytes % 16 != 0) return MOE_ERR_SHAPE;
+    if (!aligned16(buf) || (reinterpret_cast<uintptr_t>(sink) & 3u) != 0) return MOE_ERR_ALIGN;
+    int sms = 0;
+    if (const int st = device_sms(&sms); st != MOE_OK) return st;
+    return cuda_status(launch_stream_read(buf, bytes, sink, sms, static_cast<cudaStream_t>(stream)));
+}
+
 int moe_test_barrier_timeout(int enable) {
     set_test_barrier_timeout(enable != 0);
     return MOE_OK;

@@ -118,6 +118,9 @@ cudaError_t launch_router(const __nv_bfloat16* x, int T, int H, const __nv_bfloa
 // (x [T][K], w [N][K], N % 16 == 0, K % 32 == 0; the router's logits kernel).
 cudaError_t launch_dense_bf16(const __nv_bfloat16* x, int T, int K, const __nv_bfloat16* w, int N, float* part,
                               int KS, cudaStream_t stream);
+// Plain streaming read of [p, p + bytes) (bytes a positive multiple of 16, p 16-byte aligned)
+// XOR-folded into *sink (stream_read.cu): the benchmark's size-matched read ceiling.
+cudaError_t launch_stream_read(const void* p, size_t bytes, uint32_t* sink, int sms, cudaStream_t stream);
 // Shared expert (shared_expert.cu): workspace bytes and the launches.
 size_t shared_expert_ws_bytes(int T, int H, int S, int sms);
 cudaError_t launch_shared_expert(const __nv_bfloat16* x, int T, int H, int S, const __nv_bfloat16* wg,

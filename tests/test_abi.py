@@ -190,3 +190,13 @@ def test_router_rejects_bad_arguments(lib):
 def test_stage_times_without_timing(lib):
     assert lib.moe_stage_times(None, None, 4) == -1
     assert capi.stage_times() == []            # timing off: nothing recorded
+
+
+def test_stream_read_rejects_bad_arguments(lib):
+    # argument checks come before any CUDA call, so they run without a GPU
+    assert lib.moe_stream_read(None, 1024, FAKE, None) == -1
+    assert lib.moe_stream_read(FAKE, 1024, None, None) == -1
+    assert lib.moe_stream_read(FAKE, 0, FAKE, None) == -2
+    assert lib.moe_stream_read(FAKE, 1000, FAKE, None) == -2
+    assert lib.moe_stream_read(ctypes.c_void_p(FAKE.value + 8), 1024, FAKE, None) == -7
+    assert lib.moe_stream_read(FAKE, 1024, ctypes.c_void_p(FAKE.value + 2), None) == -7

@@ -8,10 +8,11 @@
 //                 programmatic dependent that starts its weight stream while gate_up drains.
 //   2 <= T <= 8 : one fused cooperative launch (fused.cu): in-kernel expert grouping, gate/up +
 //                 SwiGLU, grid barrier, down + slot-order combine (after a 4-byte barrier memset).
-//   8 < T < the measured crossover (28 FP8, 18 NVFP4): even row groups of <= 8 tokens
-//                 ("forward.rs", `moe_row_groups`), each through the cooperative kernel.
-//   from the crossover on: grouped GEMMs over expert-sorted rows on the tcgen05 tensor cores
-//                 (prefill.cu; NVFP4 needs H and I multiples of 256, else it keeps the sweeps).
+//   T >= 9 (the measured crossover, kGroupedMinRows*): grouped GEMMs over expert-sorted rows on
+//                 the tcgen05 tensor cores (prefill.cu). Shapes the grouped tier does not cover
+//                 (NVFP4 with H or I not a multiple of 256; H or I above 8192; E above 4096) run as
+//                 even row groups of <= 8 tokens ("forward.rs", `moe_row_groups`), each through
+//                 the cooperative kernel.
 // The stage entry points (moe_plan, moe_*_gate_up, moe_*_down_combine) run the same work items
 // as separate kernels and give the same bits.
 #include <cmath>

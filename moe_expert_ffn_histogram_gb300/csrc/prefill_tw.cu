@@ -110,9 +110,19 @@ struct TwCfg {
 
 }  // namespace
 
+// Token-row maps of one matrix with boxes of 16, 32, ..., 128 rows (x 64 f16): a tile loads only
+// its valid rows rounded up to 16 (the width its MMAs run at), so narrow tiles of rarely routed
+// experts do not fill shared memory with rows they never read.
+#ifndef MOE_TOK_FIT
+#define MOE_TOK_FIT 1
+#endif
+struct TokMaps {
+    CUtensorMap m[8];
+};
+
 template <int KIND, int NM, int DB, int FMT>
 __global__ void __launch_bounds__(kTwThreads, 1)
-    prefill_tw_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ CUtensorMap tmTok,
+    prefill_tw_gemm_kernel(const PrefillGemmArgs p, const __grid_constant__ TokMaps tmTok,
                            const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1) {
     using Cfg = TwCfg<NM, DB, FMT>;
     constexpr int NS = Cfg::kSlots, NT = Cfg::kTokSlots, NR = Cfg::kRawStages;
@@ -189,6 +199,9 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                 decode_tile(p, tile, mt, nt);
                 const int e = p.tile_e[mt], r0 = p.tile_r0[mt];
                 const int wy = e * p.wrows + nt * 128;        // first weight row of the slab
+                // token boxes of the tile's valid rows rounded up to 16 (1..8 sixteen-row groups)
+                const int n16 = !tok ? 0 : MOE_TOK_FIT ? (min(128, p.offsets[e + 1] - r0) + 15) / 16 : 8;
+                const CUtensorMap* tmap = tok ? &tmTok.m[n16 - 1] : nullptr;
                 bool ok = true;
                 for (int kt = 0; kt < KT; ++kt, ++sc) {
                     if (static_cast<int>(sc % 2) != pw) continue;
@@ -202,10 +215,10 @@ __global__ void __launch_bounds__(kTwThreads, 1)
                             ok = false;
                             break;
                         }
-                        // rows past the expert's last row are loaded and never used
-                        mbar_arrive_expect_tx(&tfull[s], kTwTok);
-                        tma_load_2d(smem_u32(stTok(s)), &tmTok, kt * kTwSliceK, r0, &tfull[s]);
-                        tma_load_2d(smem_u32(stTok(s)) + kTwBox, &tmTok, kt * kTwSliceK + 64, r0, &tfull[s]);
+                        // rows past the expert's last row, up to the next 16, are loaded and never used
+                        mbar_arrive_expect_tx(&tfull[s], static_cast<uint32_t>(n16) * 16 * 256);
+                        tma_load_2d(smem_u32(stTok(s)), tmap, kt * kTwSliceK, r0, &tfull[s]);
+                        tma_load_2d(smem_u32(stTok(s)) + kTwBox, tmap, kt * kTwSliceK + 64, r0, &tfull[s]);
                         tok_issued[s] = u + 1;
                     } else {
                         const uint32_t r = sc % NR, u = sc / NR;
@@ -637,7 +650,7 @@ bool tw_map(CUtensorMap* m, CUtensorMapDataType dt, int elem, const void* base, 
 }
 
 template <int KIND, int NM, int DB, int FMT>
-cudaError_t launch_tw(const PrefillGemmArgs& q, const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
+cudaError_t launch_tw(const PrefillGemmArgs& q, const TokMaps& a, const CUtensorMap& w0, const CUtensorMap& w1,
                       int grid, cudaStream_t stream) {
     using Cfg = TwCfg<NM, DB, FMT>;
     cudaError_t st = cudaFuncSetAttribute(prefill_tw_gemm_kernel<KIND, NM, DB, FMT>,
@@ -671,7 +684,8 @@ cudaError_t launch_prefill_gemm_tw(int kind, const PrefillGemmArgs& p, int N_tot
         return cudaErrorMisalignedAddress;
     PrefillGemmArgs q = p;
     q.n_tiles = N_total / 128;
-    CUtensorMap ma, mw0, mw1;
+    TokMaps ma;
+    CUtensorMap mw0, mw1;
     const uint64_t wrows_all = static_cast<uint64_t>(p.experts) * p.wrows;
     const bool fp4 = p.fmt == 1;
     if (fp4 && ((reinterpret_cast<uintptr_t>(p.sf0) | reinterpret_cast<uintptr_t>(p.sf1)) & 15u))
@@ -681,9 +695,12 @@ cudaError_t launch_prefill_gemm_tw(int kind, const PrefillGemmArgs& p, int N_tot
     const uint64_t wbytes = fp4 ? p.K / 2 : p.K;
     const uint32_t wbox = fp4 ? 64 : 128;
     const CUtensorMapSwizzle wsw = fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-    const bool ok = tw_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.a, p.K, p.a_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-                    tw_map(&mw0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w0, wbytes, wrows_all, wbox, wsw) &&
-                    tw_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w1, wbytes, wrows_all, wbox, wsw);
+    bool ok = tw_map(&mw0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w0, wbytes, wrows_all, wbox, wsw) &&
+              tw_map(&mw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w1, wbytes, wrows_all, wbox, wsw);
+    // token rows (f16, 64-element boxes, 128-byte swizzle), one map per box height 16 .. 128
+    for (int i = 0; i < 8 && ok; ++i)
+        ok = encode_map_2d(&ma.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.a, p.K, p.a_rows, 64, 16 * (i + 1),
+                           CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
     if (kind == 0) return fp4 ? launch_tw<0, 2, 0, 1>(q, ma, mw0, mw1, sms, stream)
                               : launch_tw<0, 2, 0, 0>(q, ma, mw0, mw1, sms, stream);

@@ -505,3 +505,33 @@ def test_workspace_tail_sentinel_untouched(fmt, T):
     assert torch.equal(buf[n:], sentinel)
     assert torch.equal(obuf[T * wl.H:].view(torch.int16), osent.view(torch.int16))
     check_close(bf16_to_f64(out), oracle_for(wl)["out"], f"{fmt} T={T} inside its workspace")
+
+
+# expert row counts that put one m-tile of every height 1..128 (and the next tile of a
+# multi-tile expert) through the grouped tier: the token boxes are loaded with the tile's valid
+# rows rounded up to 16, one tensor map per height
+_TILE_HEIGHT_COUNTS = [1, 15, 16, 17, 31, 32, 33, 47, 48, 49, 63, 64, 65, 79, 80, 81, 95, 96, 97,
+                       111, 112, 113, 127, 128, 129, 143, 144, 255, 256, 257]
+
+
+def _routes_with_counts(counts, topk, pad_expert):
+    """Route ids [T][topk] in which expert e appears counts[e] times; the slots past the total
+    go to pad_expert. Duplicate ids within a token are legal (they are summed)."""
+    flat = np.concatenate([np.full(c, e, dtype=np.int32) for e, c in enumerate(counts)])
+    T = -(-flat.size // topk)
+    ids = np.full(T * topk, pad_expert, dtype=np.int32)
+    ids[:flat.size] = np.random.default_rng(77).permutation(flat)
+    return torch.from_numpy(ids.reshape(T, topk))
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_prefill_every_token_box_height(fmt):
+    E = len(_TILE_HEIGHT_COUNTS) + 1                 # the last expert takes the padding slots
+    ids = _routes_with_counts(_TILE_HEIGHT_COUNTS, 8, E - 1)
+    T = ids.shape[0]
+    wl = inputs.make_custom(fmt, T, 256, 256, E, seed=1234, device=DEV)
+    wl.ids = ids.to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(wl, err=err)
+    assert int(err.item()) == 0
+    check_close(bf16_to_f64(out), oracle_for(wl)["out"], f"{fmt} prefill, every token-box height")

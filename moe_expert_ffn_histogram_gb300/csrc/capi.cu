@@ -106,10 +106,11 @@ struct Ws {
     template <class P> P* at(size_t off) const { return reinterpret_cast<P*>(base + off); }
 };
 
-int check_ws(void* ws, size_t bytes, int rows, int I, int E, int topk, Ws& out) {
+// fmt: 0 FP8, 1 NVFP4 (whose layout has room for the single-token kernels' activation scales)
+int check_ws(void* ws, size_t bytes, int rows, int I, int E, int topk, int fmt, Ws& out) {
     if (ws == nullptr) return MOE_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
-    out.L = ws_layout(rows, I, E, topk);
+    out.L = ws_layout(rows, I, E, topk, fmt == 1 ? kFp4TokFeat : kFeatBlock);
     out.base = static_cast<uint8_t*>(ws);
     if (bytes < out.L.total) return MOE_ERR_WORKSPACE;
     return MOE_OK;
@@ -313,7 +314,7 @@ int forward(const uint16_t* x, int T, int H, int I, int E, int topk, const int32
     }
     const int rows_max = rows_per_sweep(T);
     Ws w;
-    if ((rc = check_ws(ws, ws_bytes, rows_max, I, E, topk, w))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, rows_max, I, E, topk, FMT, w))) return rc;
     // even split into ceil(T/8) groups, never a trailing group of one ("forward.rs",
     // `moe_row_groups`); the workspace is rebuilt per group, in stream order.
     const int ngroups = (T + kMaxRowsPerSweep - 1) / kMaxRowsPerSweep;
@@ -374,7 +375,7 @@ size_t moe_workspace_bytes(int T, int H, int I, int E, int topk, int fmt) {
     if (check_sizes(T, H, I, E, topk) != MOE_OK) return 0;
     if (uses_prefill(T, H, I, E, fmt == MOE_FMT_FP8_E4M3_B128 ? 0 : 1))
         return prefill_layout(T, H, I, E, topk).total;
-    return ws_layout(rows_per_sweep(T), I, E, topk).total;
+    return ws_layout(rows_per_sweep(T), I, E, topk, fmt == MOE_FMT_NVFP4 ? kFp4TokFeat : kFeatBlock).total;
 }
 
 int moe_route_permute(const int32_t* topk_ids, int T, int topk, int E, int32_t* counts,
@@ -517,7 +518,7 @@ int moe_plan(int T, int H, int I, int E, int topk, int fmt, const int32_t* topk_
     if (rc) return rc;
     if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
     Ws w;
-    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, fmt == MOE_FMT_NVFP4 ? 1 : 0, w))) return rc;
     return stage_plan(T, E, topk, topk_ids, w, err, static_cast<cudaStream_t>(stream));
 }
 
@@ -532,7 +533,7 @@ int moe_fp8_gate_up(const uint16_t* x, int T, int H, int I, int E, int topk,
     if (rc) return rc;
     if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
     Ws w;
-    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, 0, w))) return rc;
     return stage_gate_up<0>(x, T, H, I, E, topk, topk_ids, w_gate, s_gate, nullptr, 1.f, w_up,
                             s_up, nullptr, 1.f, limit, w, err, static_cast<cudaStream_t>(stream));
 }
@@ -546,7 +547,7 @@ int moe_fp8_down_combine(int T, int H, int I, int E, int topk, const int32_t* to
     if (rc) return rc;
     if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
     Ws w;
-    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, 0, w))) return rc;
     return stage_down<0>(T, H, I, E, topk, topk_ids, topk_weights, w_down, s_down, nullptr, 1.f,
                          out, w, static_cast<cudaStream_t>(stream));
 }
@@ -564,7 +565,7 @@ int moe_nvfp4_gate_up(const uint16_t* x, int T, int H, int I, int E, int topk,
     if (rc) return rc;
     if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
     Ws w;
-    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, 1, w))) return rc;
     return stage_gate_up<1>(x, T, H, I, E, topk, topk_ids, w_gate, nullptr, sf_gate, scale2_gate,
                             w_up, nullptr, sf_up, scale2_up, limit, w, err,
                             static_cast<cudaStream_t>(stream));
@@ -581,7 +582,7 @@ int moe_nvfp4_down_combine(int T, int H, int I, int E, int topk, const int32_t* 
     if (rc) return rc;
     if (T > kMaxRowsPerSweep) return MOE_ERR_UNSUPPORTED;
     Ws w;
-    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, w))) return rc;
+    if ((rc = check_ws(workspace, workspace_bytes, T, I, E, topk, 1, w))) return rc;
     return stage_down<1>(T, H, I, E, topk, topk_ids, topk_weights, w_down, nullptr, sf_down,
                          scale2_down, out, w, static_cast<cudaStream_t>(stream));
 }

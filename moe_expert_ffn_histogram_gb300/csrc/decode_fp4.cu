@@ -13,10 +13,10 @@
 //
 //   gate/up: rows g / g + 8 of the MMA tile are gate row n / up row n; B is x (f16 in shared
 //            memory with a power-of-two scale); writes a as f16 with one power-of-two scale per
-//            64-feature block (the format the down kernels read).
+//            kFp4TokFeat-feature block (one block per CTA; the down kernel below reads them).
 //   down:    rows g / g + 8 are output rows j0 + g / j0 + g + 8 of the slot's expert; B is the
-//            slot's activation a; the group scale also carries a's per-64 inverse scale (a lane's
-//            two groups lie in one 64-wide block).
+//            slot's activation a; the group scale also carries a's inverse block scale (a lane's
+//            two groups, 32 consecutive features, lie in one block).
 //
 // Sources: "memra-engine 0.108.0 src/bin/ep_step_fp8_gate.rs", `reference_expert` (gate, up,
 // SwiGLU, down) and `combine_down_rows_host` (slot order, separate rounded multiply and add);
@@ -37,6 +37,9 @@ namespace moe {
 namespace {
 
 constexpr int kGuB = MOE_FP4T_GU_BATCH;     // super-segments per load batch, gate/up
+constexpr int kGuWarps = kFp4TokFeat / 8;   // gate/up warps per CTA: 8 features (gate + up rows) each
+constexpr int kGuThreads = 32 * kGuWarps;
+constexpr int kGuMinBlocks = 2 * kItemThreads / kGuThreads;   // 128 registers per thread
 constexpr int kDnB = MOE_FP4T_DN_BATCH;     // the same, down
 
 __device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
@@ -81,8 +84,9 @@ __device__ __forceinline__ float2 e4m3x2_f32(uint32_t two_bytes) {
 
 // ---- gate/up ------------------------------------------------------------------------------------
 
-// grid (I / 64, topk), 8 warps: warp w computes features fb*64 + 8w .. +7 of slot blockIdx.y.
-__global__ void __launch_bounds__(kItemThreads, 2) fp4_token_gate_up_kernel(const GateUpArgs a) {
+// grid (I / kFp4TokFeat, topk), kGuWarps warps: warp w computes features fb*kFp4TokFeat + 8w .. +7
+// of slot blockIdx.y.
+__global__ void __launch_bounds__(kGuThreads, kGuMinBlocks) fp4_token_gate_up_kernel(const GateUpArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];    // x as f16 [H]
     __shared__ GateUpShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kItemThreads, 2) fp4_token_gate_up_kernel(cons
         if (e != -1 && fb == 0 && tid == 0 && a.err != nullptr) atomicOr(a.err, 1);
         return;
     }
-    const int n = fb * kFeatBlock + warp * 8 + g;
+    const int n = fb * kFp4TokFeat + warp * 8 + g;
     const size_t row = static_cast<size_t>(e) * I + n;
     const uint8_t* pg = a.wg + row * (H / 2) + c * 16;     // codes: 64 bytes per super-segment
     const uint8_t* pu = a.wu + row * (H / 2) + c * 16;
@@ -121,7 +125,7 @@ __global__ void __launch_bounds__(kItemThreads, 2) fp4_token_gate_up_kernel(cons
         const int nv = H / 8;
         const uint4* xr = reinterpret_cast<const uint4*>(a.x);
         float m = 0.0f;
-        for (int v = tid; v < nv; v += kItemThreads) {
+        for (int v = tid; v < nv; v += kGuThreads) {
             const uint4 q = __ldg(xr + v);
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -136,14 +140,14 @@ __global__ void __launch_bounds__(kItemThreads, 2) fp4_token_gate_up_kernel(cons
         __syncthreads();
         if (tid == 0) {
             float mm = 0.0f;
-            for (int w = 0; w < kItemWarps; ++w) mm = fmaxf(mm, sh.red[w][0]);
+            for (int w = 0; w < kGuWarps; ++w) mm = fmaxf(mm, sh.red[w][0]);
             float inv;
             sh.a_scale[0] = pow2_range_scale(mm, inv);
             sh.x_inv[0] = inv;
         }
         __syncthreads();
         const float s = sh.a_scale[0];
-        for (int v = tid; v < nv; v += kItemThreads) {
+        for (int v = tid; v < nv; v += kGuThreads) {
             const uint4 q = __ldg(xr + v);
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
             uint32_t o[4];
@@ -228,10 +232,10 @@ __global__ void __launch_bounds__(kItemThreads, 2) fp4_token_gate_up_kernel(cons
     __syncthreads();
     float mm = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kItemWarps; ++w) mm = fmaxf(mm, sh.red[w][1]);
+    for (int w = 0; w < kGuWarps; ++w) mm = fmaxf(mm, sh.red[w][1]);
     float inv;
     const float s_a = pow2_range_scale(mm, inv);
-    if (tid == 0) a.act_scale[static_cast<size_t>(slot) * (I / kFeatBlock) + fb] = inv;
+    if (tid == 0) a.act_scale[static_cast<size_t>(slot) * (I / kFp4TokFeat) + fb] = inv;
     if (c == 0) a.act[static_cast<size_t>(slot) * I + n] = __float2half_rn(hv * s_a);
 }
 
@@ -260,7 +264,8 @@ __global__ void __launch_bounds__(kItemThreads, 3) fp4_token_down_kernel(const D
         const int hx = g - 2 * c;
         const bool carrier = hx == 0 || hx == 1;
         const __half* hb = a.act + static_cast<size_t>(k) * I + c * 32 + (hx == 1 ? 16 : 0);
-        const float* hs = a.act_scale + static_cast<size_t>(k) * (I / kFeatBlock) + (c >> 1);
+        // the scale block of the lane's 32 features c*32 .. c*32+31 of each 128-wide super-segment
+        const float* hs = a.act_scale + static_cast<size_t>(k) * (I / kFp4TokFeat) + (32 * c) / kFp4TokFeat;
 
         uint4 qa[kDnB], qb[kDnB], xa[kDnB][2];
         uint32_t sa[kDnB], sb[kDnB];
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(kItemThreads, 3) fp4_token_down_kernel(const D
                         xa[s][0] = *reinterpret_cast<const uint4*>(hb + (t0 + s) * 128);
                         xa[s][1] = *reinterpret_cast<const uint4*>(hb + (t0 + s) * 128 + 8);
                     }
-                    ai[s] = hs[2 * (t0 + s)];                  // a's scale of the lane's 64-block
+                    ai[s] = hs[(128 / kFp4TokFeat) * (t0 + s)];   // a's scale of the lane's block
                 }
         };
         auto load_w = [&](int cnt) {
@@ -378,7 +383,7 @@ cudaError_t launch_fp4_token_gate_up(const GateUpArgs& a, int topk, cudaStream_t
                                                     static_cast<int>(smem));
         if (st != cudaSuccess) return st;
     }
-    fp4_token_gate_up_kernel<<<dim3(a.I / kFeatBlock, topk), kItemThreads, smem, stream>>>(a);
+    fp4_token_gate_up_kernel<<<dim3(a.I / kFp4TokFeat, topk), kGuThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

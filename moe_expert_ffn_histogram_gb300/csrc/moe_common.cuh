@@ -18,6 +18,14 @@ namespace moe {
 constexpr int kMaxTopk = 8;
 constexpr int kMaxCols = 8;          // B columns per MMA tile (n = 8)
 constexpr int kFeatBlock = 64;       // features per gate/up CTA, = K width of one a-scale block
+// features per single-token NVFP4 gate/up CTA (decode_fp4.cu), = the K width of its a-scale
+// blocks: 32 spreads the 2 x 8 x I/16 warps of one token over 4-warp CTAs (several per SM, so
+// that no SM carries twice the loads of another); 64 is the 8-warp layout of the other kernels
+#ifndef MOE_FP4T_FEAT
+#define MOE_FP4T_FEAT 32
+#endif
+constexpr int kFp4TokFeat = MOE_FP4T_FEAT;
+static_assert(kFp4TokFeat == 32 || kFp4TokFeat == 64, "single-token NVFP4 feature block");
 constexpr int kDownRows = 16;        // output rows per down/combine CTA
 constexpr int kPlanThreads = 1024;
 constexpr int kMaxPlanExperts = 4096;
@@ -34,8 +42,10 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// rows: tokens handled per sub-batch (<= 8); pairs = rows * topk.
-__host__ __device__ inline WsLayout ws_layout(int rows, int I, int E, int topk) {
+// rows: tokens handled per sub-batch (<= 8); pairs = rows * topk. act_blk: the K width of one
+// activation-scale block (kFeatBlock; NVFP4 banks reserve room for kFp4TokFeat-wide blocks, which
+// the single-token kernels write).
+__host__ __device__ inline WsLayout ws_layout(int rows, int I, int E, int topk, int act_blk = kFeatBlock) {
     const size_t P = static_cast<size_t>(rows) * topk;
     WsLayout L{};
     size_t o = 0;
@@ -50,7 +60,7 @@ __host__ __device__ inline WsLayout ws_layout(int rows, int I, int E, int topk) 
     L.sorted_pair = take(P * 4);
     L.pair_to_sorted = take(P * 4);
     L.act = take(P * static_cast<size_t>(I) * 2);
-    L.act_scale = take(P * static_cast<size_t>(I / kFeatBlock) * 4);
+    L.act_scale = take(P * static_cast<size_t>(I / (act_blk < kFeatBlock ? act_blk : kFeatBlock)) * 4);
     L.total = o;
     return L;
 }

@@ -131,3 +131,15 @@ def test_sweep_rows_even_split():
     for T in range(1, 300):
         r = bench.sweep_rows(T)
         assert sum(r) == T and len(r) == (T + 7) // 8 and max(r) - min(r) <= 1 and max(r) <= 8
+
+
+def test_ceiling_entry_ratio_and_fraction():
+    """The size-matched read ceiling: bytes / read time against the peak, and the read time over
+    the measured time (1.0 = the kernel or step ran as fast as a plain read of its bytes)."""
+    e = bench.ceiling_entry(352_436_288, 72.3, 61.44, 6773.5, "step_vs_read")
+    assert e["bytes"] == 352_436_288
+    assert e["read_gbs"] == pytest.approx(352_436_288 / 61.44e-6 / 1e9, rel=1e-3)
+    assert e["read_frac_of_peak"] == pytest.approx(352_436_288 / 61.44e-6 / 1e9 / 6773.5, abs=1e-4)
+    assert e["step_vs_read"] == pytest.approx(61.44 / 72.3, abs=1e-4)
+    # a step slower than the read reports a ratio below 1
+    assert bench.ceiling_entry(1 << 20, 10.0, 5.0, 1000.0, "kernel_vs_read")["kernel_vs_read"] == 0.5

@@ -22,7 +22,7 @@ struct GateUpArgs {
     float limit;
     Groups grp;
     __half* act;          // [P][I] f16, range-scaled
-    float* act_scale;     // [P][I/64] inverse range scale
+    float* act_scale;     // [P][I/64] inverse range scale ([P][I/32] in the single-token NVFP4 kernels)
     int32_t* err;
     // Single-token NVFP4 calls whose weights fit in L2: each CTA first asks L2 for its own gate/up
     // rows and for its share of its expert's down matrix (bulk prefetch), so that HBM streams the
@@ -56,7 +56,7 @@ struct DownArgs {
     int s2_stride;
     Groups grp;
     const __half* act;      // [P][I]
-    const float* act_scale; // [P][I/64]
+    const float* act_scale; // [P][I/64] ([P][I/32] in the single-token NVFP4 kernels)
     __nv_bfloat16* out;     // [T][H]
     // layer epilogue (nullable): out = bf16((sum_k w*y + shared) + residual), fp32 adds in that order
     const __nv_bfloat16* shared;     // [T][H] shared-expert output

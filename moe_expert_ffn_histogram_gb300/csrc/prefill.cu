@@ -296,7 +296,7 @@ cudaError_t launch_prefill(int fmt, const __nv_bfloat16* x, int T, int H, int I,
     gu.sorted_pair = I32(L.sorted_pair);
     gu.topk = topk;
     gu.K = H;
-    gu.n_tiles = I / 64;
+    gu.n_tiles = I / prefill::kBN;
     gu.a = x16;
     gu.a_inv = xinv;
     gu.w0 = wg;

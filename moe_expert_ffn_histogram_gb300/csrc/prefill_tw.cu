@@ -110,12 +110,14 @@ struct TwCfg {
 
 }  // namespace
 
-// Token-row maps of one matrix with boxes of 16, 32, ..., 128 rows (x 64 f16): a tile loads only
-// its valid rows rounded up to 16 (the width its MMAs run at), so narrow tiles of rarely routed
-// experts do not fill shared memory with rows they never read.
+// 1: a tile's token boxes hold its valid rows rounded up to 16; 0: always 128 rows.
 #ifndef MOE_TOK_FIT
 #define MOE_TOK_FIT 1
 #endif
+
+// Token-row maps of one matrix with boxes of 16, 32, ..., 128 rows (x 64 f16): a tile loads only
+// its valid rows rounded up to 16 (the width its MMAs run at), so narrow tiles of rarely routed
+// experts do not fill shared memory with rows they never read.
 struct TokMaps {
     CUtensorMap m[8];
 };

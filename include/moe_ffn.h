@@ -161,7 +161,8 @@ MOE_API int moe_fp8_forward(const uint16_t* x, int T, int H, int I, int E, int t
  * multiples of 256, otherwise T > 8 runs as sweeps of <= 8 tokens through the cooperative kernel.
  * Arithmetic: an E2M1 code times its E4M3 scale is exact in f16, so every stage scales each code
  * in f16 with no rounding, except a single token's gate/up, which scales each 16-wide group's
- * fp32 partial sum once. scale_2 and the activation scales apply in fp32.
+ * fp32 partial sum once (and gives its activation a one power-of-two scale per 32-wide block
+ * instead of 64). scale_2 and the activation scales apply in fp32.
  */
 MOE_API int moe_nvfp4_forward(const uint16_t* x, int T, int H, int I, int E, int topk,
                       const int32_t* topk_ids, const float* topk_weights,

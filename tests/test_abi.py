@@ -67,6 +67,18 @@ def test_workspace_bytes_is_pure_and_monotone(lib):
     assert capi.workspace_bytes(1, 256, 128, 16, 8, 7) == 0
 
 
+def test_nvfp4_workspace_holds_the_single_token_activation_scales(lib):
+    """One NVFP4 token's gate/up writes one activation scale per 32 features (FP8: per 64), so its
+    workspace's scale region holds topk * I/32 fp32 values instead of topk * I/64 (each region is
+    rounded up to 256 bytes); everything else is the same."""
+    def ru(n):
+        return (n + 255) // 256 * 256
+    for H, I in [(5120, 1536), (7168, 2048), (256, 128), (512, 8192)]:
+        f8 = capi.workspace_bytes(1, H, I, 160, 8, capi.FMT_FP8)
+        f4 = capi.workspace_bytes(1, H, I, 160, 8, capi.FMT_NVFP4)
+        assert f4 - f8 == ru(8 * (I // 32) * 4) - ru(8 * (I // 64) * 4)
+
+
 FAKE = ctypes.c_void_p(0x10000000)     # never dereferenced: every call below fails its checks
 
 

@@ -93,6 +93,15 @@ def test_topk_below_eight(fmt):
     check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"{fmt} topk=3")
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("T,topk", [(1, 1), (1, 3), (1, 5), (40, 1), (40, 5)])
+def test_topk_below_eight_single_token_and_grouped(fmt, T, topk):
+    """Fewer than 8 slots through the single-token kernels (T = 1: a grid row per slot, the down
+    kernel's warps past topk idle) and the grouped tier (T = 40: P = T * topk sorted rows)."""
+    wl = inputs.make_custom(fmt, T, 512, 256, 12, seed=70 + 10 * T + topk, device=DEV, topk=topk)
+    check_close(bf16_to_f64(run(wl)), oracle_for(wl)["out"], f"{fmt} T={T} topk={topk}")
+
+
 def test_tiny_fp8_decode_config():
     wl = inputs.make_workload("tiny_fp8_decode", device=DEV)
     assert wl.ids.tolist() == [[0, 2, 4, 6, 8, 10, 12, 14]]
